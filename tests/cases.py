@@ -1,0 +1,18 @@
+"""Reduced workloads that the fp64 oracle finishes in seconds.
+
+Each keeps the structure of one of the five full workloads (dtypes, layout,
+shared expert, replica map, router) at sizes that still span several 128-wide
+tiles and leave a ragged tail."""
+from moe_inputs import CONFIGS
+
+SMALL = {
+    "tiny": CONFIGS["tiny"],
+    "bf16_masked": CONFIGS["mixtral_decode"].replace(
+        name="bf16_masked", T=24, H=256, I=384, E=8, K=2, M_max=24),
+    "e4m3_masked_shared": CONFIGS["dsv3_decode"].replace(
+        name="e4m3_masked_shared", T=40, H=384, I=256, E=16, K=4, M_max=40),
+    "e4m3_eplb_zipf": CONFIGS["skew_eplb"].replace(
+        name="e4m3_eplb_zipf", T=48, H=256, I=384, E=16, K=4, M_max=48, redundant=4),
+    "e4m3_contig": CONFIGS["prefill"].replace(
+        name="e4m3_contig", T=64, H=256, I=256, E=32, K=4),
+}

@@ -1,0 +1,358 @@
+"""Pins of the CPU oracle to facts fixed outside the oracle itself.
+
+Each test checks the oracle against one of: a worked example printed on the
+pages, a library routine the step reduces to, a closed form, a conservation
+law the pages state, or brute force on tiny inputs.  A plausible slip in the
+oracle (a dropped term, a swapped gate/up, a transposed weight, a wrong tie
+rule, a wrong rounding) fails at least one of them."""
+import itertools
+import json
+import os
+
+import numpy as np
+import pytest
+import scipy.special
+import torch
+
+import moe_inputs as mi
+import oracle
+from cases import SMALL
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+# ---- EPLB maps (vLLM EPLB, section 1.2, worked example) --------------------
+
+def test_eplb_worked_example():
+    g = json.load(open(os.path.join(GOLDEN, "eplb_worked_example.json")))
+    E = g["num_logical_experts"]
+    for case in g["cases"]:
+        l2p, rc, r = oracle.eplb_invert(case["physical_to_logical_map"], E)
+        assert l2p.tolist() == case["logical_to_physical_map"]
+        assert rc.tolist() == case["logical_replica_count"]
+        assert r == max(case["logical_replica_count"])
+
+
+def test_eplb_rejects_bad_map():
+    with pytest.raises(ValueError):
+        oracle.eplb_invert([0, 1, 4], 4)
+    with pytest.raises(ValueError):
+        oracle.eplb_invert([0, 0, 0], 2, R=2)
+
+
+# ---- routing ---------------------------------------------------------------
+
+def _ref_route(logits, K):
+    """Library reference: stable argsort on -logit, scipy softmax over all E,
+    renormalised over the chosen K."""
+    ids = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :K]
+    p = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    pk = np.take_along_axis(p, ids, axis=1)
+    return ids, pk / pk.sum(axis=1, keepdims=True)
+
+
+@pytest.mark.parametrize("T,E,K", [(16, 8, 2), (33, 256, 8), (20, 512, 10), (5, 4, 4), (7, 6, 1)])
+def test_route_matches_library(T, E, K):
+    logits = mi.normal(3, 99, (T, E), dtype="f32")
+    ids, w = oracle.route(logits, K)
+    rid, rw = _ref_route(logits, K)
+    assert (ids == rid).all()
+    np.testing.assert_allclose(w, rw, rtol=1e-13, atol=1e-15)
+
+
+def test_route_special_cases():
+    rng = np.random.default_rng(0)
+    logits = rng.standard_normal((9, 6)).astype(np.float32)
+    # K = E: every expert, weights = the full softmax
+    ids, w = oracle.route(logits, 6)
+    full = scipy.special.softmax(logits.astype(np.float64), axis=1)
+    np.testing.assert_allclose(w, np.take_along_axis(full, ids, 1), rtol=1e-13)
+    # K = 1: weight 1
+    _, w1 = oracle.route(logits, 1)
+    assert (w1 == 1.0).all()
+    # equal logits: ids 0..K-1 (ties to the lower index), equal weights
+    ids, w = oracle.route(np.zeros((3, 8), np.float32), 3)
+    assert ids.tolist() == [[0, 1, 2]] * 3
+    np.testing.assert_allclose(w, 1.0 / 3.0, rtol=1e-15)
+    # partial ties: lower index first among equal logits
+    l = np.array([[1.0, 3.0, 3.0, 2.0, 3.0]], np.float32)
+    ids, _ = oracle.route(l, 4)
+    assert ids.tolist() == [[1, 2, 4, 3]]
+
+
+def test_route_top2_then_softmax_equivalence():
+    """Mixtral computes top-2 first and a softmax over those two logits; the
+    softmax-then-renormalise form gives the same weights."""
+    logits = mi.normal(5, 7, (50, 8), dtype="f32")
+    ids, w = oracle.route(logits, 2)
+    top = np.take_along_axis(logits.astype(np.float64), ids, 1)
+    np.testing.assert_allclose(w, scipy.special.softmax(top, axis=1), rtol=1e-13)
+
+
+# ---- codecs -----------------------------------------------------------------
+
+def test_e4m3_decode_all_codes():
+    codes = np.arange(256, dtype=np.uint8)
+    v = oracle.e4m3_decode(codes)
+    lib = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    nan = np.isnan(lib)
+    assert (np.isnan(v) == nan).all() and nan.sum() == 2  # S.1111.111
+    assert (v[~nan] == lib[~nan]).all()
+    # constants of the OCP E4M3 format
+    assert v[0x7E] == 448.0 and v[0x01] == 2.0 ** -9 and v[0x08] == 2.0 ** -6 and v[0x38] == 1.0
+    assert v[0xFE] == -448.0 and v[0x80] == 0.0
+
+
+def test_e4m3_encode_rne_satfinite():
+    fin = oracle.e4m3_decode(np.arange(0, 0x7F, dtype=np.uint8))
+    mids = (fin[:-1] + fin[1:]) / 2.0  # exact ties
+    rng = np.random.default_rng(1)
+    vals = np.concatenate([fin, mids, -mids, rng.standard_normal(20000) * 50,
+                           rng.standard_normal(2000) * 1e-3, [449.0, 463.9, 470.0, 1e6, -1e6, -0.0]])
+    vals = vals.astype(np.float32)
+    got = oracle.e4m3_encode(vals)
+    ref = torch.from_numpy(vals).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    assert (got == ref).all()
+    # ties go to the even code
+    tie = oracle.e4m3_encode(np.array([(1.0 + 1.125) / 2, (1.125 + 1.25) / 2], np.float32))
+    assert tie.tolist() == [0x38, 0x3A]
+
+
+def test_bf16_encode_rne():
+    rng = np.random.default_rng(2)
+    base = rng.standard_normal(50000).astype(np.float32)
+    bits = base.view(np.uint32)
+    ties = ((bits & 0xFFFF0000) | 0x8000).view(np.float32)  # exactly half an ulp
+    vals = np.concatenate([base, ties, np.float32([1e-40, 3.4e38, 0.0, -0.0])])
+    got = oracle.bf16_encode(vals.astype(np.float64))
+    ref = torch.from_numpy(vals).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert (got == ref).all()
+
+
+def test_quant_rows_reduces_to_library_calls():
+    """The 1x128 rule is fp32 division by amax/448 and an RNE satfinite cast."""
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal((6, 512)).astype(np.float32)
+    x[2, 128:256] = 0.0
+    q, s = oracle.quant_rows_e4m3(x)
+    xt = torch.from_numpy(x).view(6, 4, 128)
+    amax = xt.abs().amax(-1)
+    sref = torch.where(amax == 0, torch.ones_like(amax), amax / torch.tensor(448.0, dtype=torch.float32))
+    qref = (xt / sref[..., None]).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+    assert (s == sref.numpy()).all()
+    assert (q == qref.reshape(6, 512).numpy()).all()
+    # the largest element of a group maps to +-448 exactly
+    g = x[0, :128]
+    i = np.argmax(np.abs(g))
+    assert q[0, i] in (0x7E, 0xFE)
+    assert s[2, 1] == 1.0 and (q[2, 128:256] == 0).all()
+
+
+# ---- layout -----------------------------------------------------------------
+
+def _brute_layout(cfg, ids, p2l):
+    """Definition on tiny inputs: slot by replica round-robin, rows of a slot
+    listed by ascending token index."""
+    T, K = ids.shape
+    P, S = cfg.P, cfg.S
+    if p2l is None:
+        slot = lambda t, e: e
+    else:
+        reps = {e: [s for s in range(P) if p2l[s] == e] for e in range(cfg.E)}
+        slot = lambda t, e: reps[e][t % len(reps[e])]
+    members = {s: [] for s in range(P + S)}
+    for t in range(T):
+        for k in range(K):
+            members[slot(t, ids[t, k])].append((t, k))
+        if S:
+            members[P].append((t, K))
+    counts = [len(members[s]) for s in range(P + S)]
+    offsets = [0] + list(itertools.accumulate(counts))
+    row_of = np.zeros((T, K + S), np.int64)
+    for s in range(P + S):
+        for rank, (t, k) in enumerate(sorted(members[s])):
+            row_of[t, k] = s * cfg.M_max + rank if cfg.layout == "masked" else offsets[s] + rank
+    return np.array(counts), np.array(offsets), row_of
+
+
+@pytest.mark.parametrize("layout", ["masked", "contig"])
+@pytest.mark.parametrize("shared", [0, 1])
+@pytest.mark.parametrize("use_map", [False, True])
+def test_layout_brute_force(layout, shared, use_map):
+    rng = np.random.default_rng(4)
+    for trial in range(40):
+        E = int(rng.integers(1, 5))
+        K = int(rng.integers(1, E + 1))
+        T = int(rng.integers(1, 7))
+        extra = int(rng.integers(0, 3)) if use_map else 0
+        cfg = SMALL["tiny"].replace(T=T, E=E, K=K, shared=shared, layout=layout, M_max=T if layout == "masked" else 0,
+                                    redundant=extra)
+        ids = np.stack([rng.permutation(E)[:K] for _ in range(T)]).astype(np.int32)
+        p2l = None
+        if use_map:
+            p2l = np.concatenate([np.arange(E), rng.integers(0, E, extra)]).astype(np.int32)
+            rng.shuffle(p2l)
+        got = oracle.layout(cfg, ids, p2l)
+        assert got["status"] == 0
+        counts, offsets, row_of = _brute_layout(cfg, ids, p2l)
+        assert (got["masked_m"] == counts).all()
+        assert (got["offsets"] == offsets).all()
+        assert (got["row_of"] == row_of).all()
+        # src_of inverts row_of on every written row
+        for t in range(T):
+            for r in got["row_of"][t]:
+                assert got["src_of"][r] == t
+
+
+def test_counts_conserved_and_replicas_sum():
+    """MoonEP 'Why dynamic routing is hard': per-expert counts sum to the
+    number of routed records (R=1 here: T*K); replica counts sum to the
+    logical count; the shared slot holds every token."""
+    cfg = SMALL["e4m3_eplb_zipf"]
+    x, logits = mi.activations(cfg)
+    ids, _ = oracle.route(logits, cfg.K)
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    p2l = mi.replica_map(counts, cfg.E, cfg.redundant)
+    lay = oracle.layout(cfg, ids, p2l)
+    mm = lay["masked_m"]
+    assert mm[:cfg.P].sum() == cfg.T * cfg.K
+    assert mm[cfg.P] == cfg.T
+    per_logical = np.bincount(p2l, weights=mm[:cfg.P], minlength=cfg.E)
+    assert (per_logical == counts).all()
+    # replica of record (t, k) is the (t mod replica_count)-th slot of its expert
+    l2p, rc, _ = oracle.eplb_invert(p2l, cfg.E)
+    for t in range(cfg.T):
+        for k in range(cfg.K):
+            e = ids[t, k]
+            assert lay["slot_of"][t, k] == l2p[e, t % rc[e]]
+
+
+def test_layout_overflow_and_bad_ids():
+    cfg = SMALL["tiny"].replace(T=4, E=2, K=1, M_max=2)
+    ids = np.zeros((4, 1), np.int32)
+    assert oracle.layout(cfg, ids)["status"] == -2      # 4 rows into M_max = 2
+    assert oracle.layout(cfg, ids + 5)["status"] == -1  # expert id out of range
+    cfg2 = cfg.replace(K=2, M_max=4)
+    assert oracle.layout(cfg2, np.zeros((4, 2), np.int32))["status"] == -3  # same expert twice
+
+
+# ---- expert FFN ---------------------------------------------------------------
+
+def _silu(z):
+    return z / (1.0 + np.exp(-z))
+
+
+@pytest.mark.parametrize("H,I", [(64, 128), (96, 40)])
+def test_single_expert_is_dense_swiglu(H, I):
+    """E = 1, K = 1: the layer is one dense SwiGLU FFN, y = W2 (silu(W1 x) * W3 x),
+    evaluated here with numpy matmuls on the math (untransposed) weights."""
+    cfg = SMALL["tiny"].replace(T=5, H=H, I=I, E=1, K=1, M_max=5)
+    x, logits = mi.activations(cfg)
+    w13, _ = mi.expert_weights(cfg, "w13")
+    w2, _ = mi.expert_weights(cfg, "w2")
+    out, exact = oracle.layer(cfg, x, logits, w13, None, w2, None)
+    W1 = w13[0, :I, :].astype(np.float64).T   # [H, I]
+    W3 = w13[0, I:, :].astype(np.float64).T   # [H, I]
+    W2 = w2[0].astype(np.float64).T           # [I, H]
+    xf = x.astype(np.float64)
+    h = (_silu(xf @ W1) * (xf @ W3)).astype(np.float32).astype(np.float64)
+    y = (h @ W2).astype(np.float32).astype(np.float64)
+    np.testing.assert_allclose(exact, y, rtol=1e-12, atol=1e-14)
+
+
+def test_closed_forms():
+    """Zero gate weights give silu(0) = 0 and a zero output; an identity-like
+    W2 (H = I, ones on the diagonal) returns h itself."""
+    cfg = SMALL["tiny"].replace(T=3, H=128, I=128, E=1, K=1, M_max=3)
+    x, logits = mi.activations(cfg)
+    w13, _ = mi.expert_weights(cfg, "w13")
+    w2 = np.eye(128, dtype=np.float32)[None]
+    z = w13.copy()
+    z[0, :128] = 0.0
+    _, ex0 = oracle.layer(cfg, x, logits, z, None, w2, None)
+    assert (ex0 == 0).all()
+    _, ex1 = oracle.layer(cfg, x, logits, w13, None, w2, None)
+    xf = x.astype(np.float64)
+    h = _silu(xf @ w13[0, :128].astype(np.float64).T) * (xf @ w13[0, 128:].astype(np.float64).T)
+    np.testing.assert_allclose(ex1, h.astype(np.float32), rtol=1e-12)
+
+
+def test_weighted_combine_and_shared_expert():
+    """Two experts plus a shared one on one token, checked by hand: out = w0 y0 + w1 y1 + y_shared."""
+    cfg = SMALL["tiny"].replace(T=1, H=128, I=128, E=3, K=2, shared=1, M_max=1)
+    x, logits = mi.activations(cfg)
+    w13, _ = mi.expert_weights(cfg, "w13")
+    w2, _ = mi.expert_weights(cfg, "w2")
+    _, exact = oracle.layer(cfg, x, logits, w13, None, w2, None)
+    ids, w = oracle.route(logits, 2)
+    xf = x[0].astype(np.float64)
+
+    def ffn(e):
+        g = w13[e, :128].astype(np.float64) @ xf
+        u = w13[e, 128:].astype(np.float64) @ xf
+        h = (_silu(g) * u).astype(np.float32).astype(np.float64)
+        return (w2[e].astype(np.float64) @ h).astype(np.float32).astype(np.float64)
+
+    ref = w[0, 0] * ffn(ids[0, 0]) + w[0, 1] * ffn(ids[0, 1]) + ffn(3)
+    np.testing.assert_allclose(exact[0], ref, rtol=1e-12)
+
+
+@pytest.mark.parametrize("name", list(SMALL))
+def test_steps_compose_to_layer(name):
+    """The per-call oracles (dispatch, gate/up, down, combine) chained over the
+    grouped layout reproduce the token-by-token layer, replicas included."""
+    cfg = SMALL[name]
+    x, logits = mi.activations(cfg)
+    w13, w13s = mi.expert_weights(cfg, "w13")
+    w2, w2s = mi.expert_weights(cfg, "w2")
+    ids, w = oracle.route(logits, cfg.K)
+    p2l = None
+    if cfg.redundant:
+        p2l = mi.replica_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.E, cfg.redundant)
+    lay = oracle.layout(cfg, ids, p2l)
+    assert lay["status"] == 0
+    order = mi.slot_experts(cfg, p2l)
+    sw13, sw2 = w13[order], w2[order]
+    sw13s = None if w13s is None else w13s[order]
+    sw2s = None if w2s is None else w2s[order]
+    xg, xgs = oracle.dispatch_values(cfg, x, lay["row_of"])
+    hg, hgs = oracle.grouped_swiglu(cfg, xg, xgs, sw13, sw13s, lay["masked_m"], lay["offsets"])
+    yg = oracle.grouped_down(cfg, hg, hgs, sw2, sw2s, lay["masked_m"], lay["offsets"])
+    out, exact = oracle.combine(cfg, yg, lay["row_of"], w.astype(np.float32))
+    lout, lexact = oracle.layer(cfg, x, logits, w13, w13s, w2, w2s)
+    scale = np.abs(lexact).max()
+    assert np.abs(exact - lexact).max() <= 1e-6 * scale
+
+
+def test_replica_invariance():
+    """A replica map changes where tokens run, not the layer's output."""
+    cfg = SMALL["e4m3_eplb_zipf"]
+    x, logits = mi.activations(cfg)
+    w13, w13s = mi.expert_weights(cfg, "w13")
+    w2, w2s = mi.expert_weights(cfg, "w2")
+    ids, w = oracle.route(logits, cfg.K)
+    outs = []
+    for p2l in (None, mi.replica_map(np.bincount(ids.ravel(), minlength=cfg.E), cfg.E, cfg.redundant)):
+        c = cfg if p2l is not None else cfg.replace(redundant=0)
+        lay = oracle.layout(c, ids, p2l)
+        order = mi.slot_experts(c, p2l)
+        xg, xgs = oracle.dispatch_values(c, x, lay["row_of"])
+        hg, hgs = oracle.grouped_swiglu(c, xg, xgs, w13[order], w13s[order], lay["masked_m"], lay["offsets"])
+        yg = oracle.grouped_down(c, hg, hgs, w2[order], w2s[order], lay["masked_m"], lay["offsets"])
+        outs.append(oracle.combine(c, yg, lay["row_of"], w.astype(np.float32))[1])
+    assert (outs[0] == outs[1]).all()
+
+
+# ---- coverage (INFRA-5, section "Batch") ----------------------------------------
+
+def test_coverage_formula_monte_carlo():
+    """Under uniform routing a batch of B tokens touches about E * C(B) experts,
+    C(B) = 1 - (1 - k/E)^B."""
+    T, E, K = 128, 256, 8
+    touched = []
+    for seed in range(12):
+        logits = mi.normal(seed, mi.STREAM_LOGITS, (T, E), dtype="f32")
+        ids, _ = oracle.route(logits, K)
+        touched.append(len(np.unique(ids)))
+    C = 1.0 - (1.0 - K / E) ** T
+    assert abs(np.mean(touched) - E * C) < 1.5
