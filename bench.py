@@ -1,0 +1,395 @@
+"""Benchmark of the single-GPU forward pass of one routed MoE layer.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl reference]
+
+One step = route -> permute -> gate/up GEMM -> down GEMM -> combine over one
+batch of the workload, inputs and weights resident in HBM, replayed from CUDA
+graphs.  Prints one JSON line (rank 0).  With N > 1 (torchrun, one rank per
+GPU) every rank runs its own replica on its own batch (no collective on the
+data path) and the whole-job throughput is the tokens of all ranks over the
+slowest rank's time.
+
+--impl reference times the CPU oracle (fp64, host cores) on a bounded sample of
+the same workload; it is the deliberately slow baseline of this repository.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+HEADLINE = "mixtral_decode"
+METRIC = "MoE layer tokens/s"
+# ncu DRAM bytes (read + write) per launch of the dominant kernel, keyed by the
+# workload and the hash of the kernel source they were captured from.
+TRAFFIC = {}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return float(d["hbm_gbs"]), float(d["bf16_tflops"]), float(d.get("bf16_tflops_sustained", d["bf16_tflops"])), "measured"
+    return 6800.0, 1900.0, 1700.0, "fallback"
+
+
+def src_hash(*names):
+    h = hashlib.sha256()
+    for n in names:
+        h.update(open(os.path.join(ROOT, "routed_expert_layer_moe_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+         "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+         "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.Q,
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        self.lines = []
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [l for l in out.splitlines() if l.strip()]
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in getattr(self, "lines", []):
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def problem_of(cfg, moe):
+    return moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, P=cfg.P, M_max=cfg.M_max,
+                            has_shared=cfg.S, act=cfg.act, wt=cfg.gemm, out=cfg.out, layout=cfg.layout)
+
+
+def to_dev(a, torch, dev):
+    a = np.ascontiguousarray(a)
+    if a.dtype == np.uint16:
+        return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(dev)
+    return torch.from_numpy(a).to(dev)
+
+
+def expert_bytes(cfg):
+    """Bytes of one expert's weights (W13 + W2, plus fp32 block scales for e4m3)."""
+    esz = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.gemm]
+    b13 = 2 * cfg.I * cfg.H * esz
+    b2 = cfg.H * cfg.I * esz
+    if cfg.gemm == "e4m3":
+        b13 += (2 * cfg.I // 128) * (cfg.H // 128) * 4
+        b2 += (cfg.H // 128) * (cfg.I // 128) * 4
+    return b13, b2
+
+
+def run_gpu(args, cfg, rank, world, local_rank):
+    import torch
+
+    import routed_expert_layer_moe_gb300 as moe
+
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    seed = rank  # each replica its own batch
+    x, logits = mi.activations(cfg, seed)
+    w13, w13s = mi.expert_weights(cfg, "w13")
+    w2, w2s = mi.expert_weights(cfg, "w2")
+    p = problem_of(cfg, moe)
+    # EPLB replica map: the hottest logical experts of this batch, counted from
+    # the GPU's own routing of it
+    p2l = None
+    if cfg.redundant:
+        pr = moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, M_max=max(cfg.M_max, 1),
+                              act=cfg.act, wt=cfg.gemm, out=cfg.out, layout=cfg.layout)
+        ids = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device=dev)
+        wts = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device=dev)
+        moe.moe_route_topk(pr, to_dev(logits, torch, dev), ids, wts)
+        counts = np.bincount(ids.cpu().numpy().ravel(), minlength=cfg.E)
+        p2l = mi.replica_map(counts, cfg.E, cfg.redundant)
+    order = torch.from_numpy(mi.slot_experts(cfg, p2l)).to(dev)
+
+    def slots(a):
+        if a is None:
+            return None
+        t = to_dev(a, torch, dev)
+        return t.index_select(0, order).contiguous() if (cfg.redundant or t.shape[0] != order.numel()) else t
+
+    L = moe.MoeLayer(p, cfg.act, cfg.gemm, cfg.out, slots(w13), slots(w2), slots(w13s), slots(w2s),
+                     phys_to_log=None if p2l is None else torch.from_numpy(p2l).to(dev), device=dev)
+    del w13, w2, w13s, w2s
+    xd, ld = to_dev(x, torch, dev), to_dev(logits, torch, dev)
+    stream = torch.cuda.Stream(dev)
+    # eager warm-up on the capture stream (first calls cache device attributes)
+    with torch.cuda.stream(stream):
+        L.forward(xd, ld, stream)
+    stream.synchronize()
+    assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
+
+    parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.swiglu(stream),
+             lambda: L.down(stream), lambda: L.combine(stream)]
+    graphs = []
+    for fn in parts:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        graphs.append(g)
+    n_launch = count_launches(cfg, p2l is not None)
+
+    def step():
+        for g in graphs:
+            g.replay()
+
+    with torch.cuda.stream(stream):
+        for _ in range(args.warmup):
+            step()
+    stream.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local_rank) as clk:
+        with torch.cuda.stream(stream):
+            for i in range(K):
+                ev[i][0].record(stream)
+                for j, g in enumerate(graphs):
+                    g.replay()
+                    ev[i][j + 1].record(stream)
+        torch.cuda.synchronize()
+    if world > 1:
+        torch.distributed.barrier()
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][4])
+    part_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(4)]
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+
+    # ---- end to end through the host: pinned inputs in, output back, every step
+    xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if x.dtype == np.uint16 else x)
+    xh = (xh.view(torch.bfloat16) if x.dtype == np.uint16 else xh).pin_memory()
+    lh = torch.from_numpy(logits).pin_memory()
+    oh = torch.empty(L.out.shape, dtype=L.out.dtype).pin_memory()
+    with torch.cuda.stream(stream):
+        for _ in range(max(1, args.warmup)):
+            xd.copy_(xh, non_blocking=True)
+            ld.copy_(lh, non_blocking=True)
+            step()
+            oh.copy_(L.out, non_blocking=True)
+    stream.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(stream):
+        e0.record(stream)
+        for _ in range(K):
+            xd.copy_(xh, non_blocking=True)
+            ld.copy_(lh, non_blocking=True)
+            step()
+            oh.copy_(L.out, non_blocking=True)
+        e1.record(stream)
+    stream.synchronize()
+    e2e_ms = e0.elapsed_time(e1)
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
+
+    mm = L.masked_m.cpu().numpy()
+    touched = int((mm > 0).sum())
+    return dict(total_ms=total_ms, part_ms=part_ms, e2e_ms=e2e_ms, masked_m=mm, touched=touched, clocks=clk.summary(),
+                n_launch=n_launch, h2d=xh.numel() * xh.element_size() + lh.numel() * lh.element_size(),
+                d2h=oh.numel() * oh.element_size(), x=x, logits=logits)
+
+
+def count_launches(cfg, with_map):
+    """Kernels (and memsets) one step enqueues: route 1; permute memset + [map] + mark + scan + scatter;
+    gate/up 1; down 1 (+ memset of the split-K counters when it splits); combine 1."""
+    n = 1 + 4 + (1 if with_map else 0) + 1 + 1 + 1
+    return n
+
+
+def gateup_roofline(cfg, res, peaks, moe_src):
+    """Algorithmic bytes of one gate/up launch: the W13 (+ scales) of every slot
+    with rows, the grouped activations it reads and the Hg it writes."""
+    hbm, _, _, src = peaks
+    b13, _ = expert_bytes(cfg)
+    mm = res["masked_m"]
+    rows = int(mm.sum())
+    esz = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.gemm]
+    act = rows * cfg.H * esz + rows * cfg.I * esz
+    if cfg.gemm == "e4m3":
+        act += rows * (cfg.H // 128 + cfg.I // 128) * 4
+    algo = res["touched"] * b13 + act
+    dur_s = res["part_ms"][1] * 1e-3
+    achieved = algo / dur_s / 1e9
+    key = "%s:%s" % (cfg.name, moe_src)
+    traffic = TRAFFIC.get(key)
+    return {"bound": "hbm", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)", "achieved": round(achieved, 1),
+            "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
+            "algorithmic_bytes": int(algo), "avg_launch_us": round(dur_s * 1e6, 2), "peak_source": src}
+
+
+def cpu_baseline(cfg, x, logits, budget_s=12.0):
+    """The oracle on the host cores, whole-layer tokens/s on a bounded sample of tokens."""
+    import oracle
+
+    w13, w13s = mi.expert_weights(cfg, "w13")
+    w2, w2s = mi.expert_weights(cfg, "w2")
+    t0 = time.time()
+    oracle.layer(cfg, x, logits, w13, w13s, w2, w2s, tokens=np.array([0], np.int32))
+    one = max(time.time() - t0, 1e-3)
+    n = int(max(1, min(cfg.T, budget_s / one)))
+    toks = np.arange(n, dtype=np.int32)
+    t0 = time.time()
+    oracle.layer(cfg, x, logits, w13, w13s, w2, w2s, tokens=toks)
+    dt = time.time() - t0
+    return {"value": round(n / dt, 3), "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": "%d of the %d tokens of one %s batch, whole layer per token, fp64" % (n, cfg.T, cfg.name)}
+
+
+def run_reference(args, cfg, rank):
+    """The oracle as the reference arm: each step is a bounded sample of tokens."""
+    import oracle
+
+    x, logits = mi.activations(cfg, 0)
+    w13, w13s = mi.expert_weights(cfg, "w13")
+    w2, w2s = mi.expert_weights(cfg, "w2")
+    t0 = time.time()
+    oracle.layer(cfg, x, logits, w13, w13s, w2, w2s, tokens=np.array([0], np.int32))
+    one = max(time.time() - t0, 1e-3)
+    total_budget = 150.0
+    per_step = max(1, min(cfg.T, int(total_budget / max(1, args.steps + args.warmup) / one)))
+    toks = np.arange(per_step, dtype=np.int32)
+    for _ in range(args.warmup):
+        oracle.layer(cfg, x, logits, w13, w13s, w2, w2s, tokens=toks)
+    t0 = time.time()
+    for _ in range(args.steps):
+        oracle.layer(cfg, x, logits, w13, w13s, w2, w2s, tokens=toks)
+    dt = time.time() - t0
+    value = per_step * args.steps / dt
+    sample = "%d of the %d tokens of one %s batch per step, whole layer per token, fp64" % (per_step, cfg.T, cfg.name)
+    return {"impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_dict(cfg, args.gpus),
+            "cpu_baseline": {"value": round(value, 3), "unit": "tokens/s", "cores": oracle.num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 3), "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def config_dict(cfg, n):
+    return {"workload": cfg.name, "description": cfg.description, "tokens_per_step": cfg.T, "H": cfg.H, "I": cfg.I,
+            "E": cfg.E, "K": cfg.K, "shared_experts": cfg.S, "physical_slots": cfg.P, "layout": cfg.layout,
+            "M_max": cfg.M_max, "expert_dtype": cfg.gemm, "parallelism": "replicas%d" % n if n > 1 else "single-gpu",
+            "l2": "expert weights exceed L2 (129 MB), no flush" if expert_bytes(cfg)[0] * cfg.E > 2 * 129e6
+            else "small workload: L2-resident (launch-latency bound)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", default=HEADLINE, choices=list(mi.CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    cfg = mi.CONFIGS[args.config]
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, cfg, rank)), flush=True)
+        return
+
+    if world > 1:
+        import torch
+        torch.cuda.set_device(local_rank)
+        torch.distributed.init_process_group("nccl")
+    peaks = load_peaks()
+    res = run_gpu(args, cfg, rank, world, local_rank)
+    if rank == 0:
+        K = args.steps
+        ms = res["total_ms"] / K
+        value = world * cfg.T * K / (res["total_ms"] * 1e-3)
+        e2e = world * cfg.T * K / (res["e2e_ms"] * 1e-3)
+        moe_src = src_hash("gemm_tc.cu", "common.cuh")
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": cfg.gemm, "data": "synthetic (seeded generator, random-init experts)",
+            "config": config_dict(cfg, world),
+            "roofline": gateup_roofline(cfg, res, peaks, moe_src),
+            "step_breakdown_us": {"route+permute": round(res["part_ms"][0] * 1e3, 2),
+                                  "gate_up": round(res["part_ms"][1] * 1e3, 2),
+                                  "down": round(res["part_ms"][2] * 1e3, 2),
+                                  "combine": round(res["part_ms"][3] * 1e3, 2)},
+            "touched_slots": res["touched"],
+            "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
+                    "d2h_bytes_per_step": res["d2h"]},
+            "gpu_launches": res["n_launch"] * K,
+            "clocks": res["clocks"],
+        }
+        b13, b2 = expert_bytes(cfg)
+        layer_bytes = res["touched"] * (b13 + b2)
+        line["layer_hbm"] = {"touched_expert_bytes": int(layer_bytes),
+                             "achieved_GBps": round(layer_bytes / (ms * 1e-3) / 1e9, 1),
+                             "frac_of_peak": round(layer_bytes / (ms * 1e-3) / 1e9 / peaks[0], 4)}
+        if world == 1 and not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline(cfg, res["x"], res["logits"])
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,206 @@
+/*
+ * moe.h -- C ABI of the single-GPU forward pass of one routed
+ * Mixture-of-Experts layer (GB300, sm_103a).
+ *
+ * The forward pass is five calls, made in this order on one stream:
+ *
+ *   moe_route_topk          softmax top-K routing of the router logits
+ *   moe_permute             counts, offsets, row maps; dispatch of the
+ *                           activations into the expert-grouped buffer
+ *   moe_grouped_swiglu_gemm per-expert gate/up GEMM with SiLU(gate) * up
+ *   moe_grouped_down_gemm   per-expert down GEMM
+ *   moe_combine             weighted sum of each token's expert outputs
+ *
+ * Sources, by page title and section:
+ *   "MoE inference and expert parallelism" (blog.vllbc.top): the routing
+ *     section and Table 3-1 (softmax top-K with renormalisation, SwiGLU experts
+ *     with W1/W3 = gate/up and W2 = down, moe_sum, DeepSeek-V3 shared expert,
+ *     Eq. 12) and the forward-pass section (fused_topk -> moe_align_block_size
+ *     -> W1/W3 GEMM -> activation -> W2 GEMM -> moe_sum).
+ *   "Inference INFRA methodology (5): MoE inference -- Batch, DeepEP, DeepGEMM
+ *     and load balancing" (yfxerp.com): section "DeepGEMM" (static
+ *     [E_loc, M_max, K] buffer with a device-resident masked_m read at run
+ *     time, no MMA for tiles that hold only padding, FP8 with the 128-wide K
+ *     promotion to FP32, contiguous layout for prefill).
+ *   "vLLM EPLB" (pnsm.cn): section 1.2 (physical_to_logical_map,
+ *     logical_to_physical_map, logical_replica_count).
+ *   "MoonEP: dynamic redundant experts" (wineandchord.com): sections "Why
+ *     dynamic routing is hard" (counts sum to the routed records) and
+ *     "Zero-copy and static buffer" (offsets / cu_seqlens, padding described
+ *     by the plan).
+ *
+ * Conventions shared by every call
+ *   - All data pointers are DEVICE pointers unless a comment says otherwise.
+ *     The caller allocates and owns every buffer, including the workspace.
+ *     The library never allocates, frees or synchronises; every call only
+ *     enqueues kernels (and memsets) on `stream`, so a sequence of calls can be
+ *     captured in a CUDA graph once the first call on the device has been made
+ *     outside of capture (it caches device attributes).
+ *   - Return status: checked on the host from the arguments and from the
+ *     launch; nothing is enqueued when a call returns MOE_ERR_INVALID or
+ *     MOE_ERR_UNSUPPORTED.  Data-dependent problems found on the device set
+ *     bits of the caller's int32 `err_flag` (MOE_FLAG_*); tokens are never
+ *     dropped silently.
+ *   - Layouts are row-major.  Counts: T tokens, H hidden, I expert
+ *     intermediate, E logical routed experts, K experts per token, P physical
+ *     slots (P == E without a replica map), S = has_shared (0/1).  The shared
+ *     expert, when present, is slot P.
+ *   - Dtypes: bf16 is IEEE binary32's upper half, e4m3 is OCP FP8 E4M3.
+ *     Supported combinations (act / wt / out): F32/F32/F32, BF16/BF16/BF16,
+ *     BF16/E4M3/BF16.  `wt` is the type of the expert weights and of the
+ *     grouped activations Xg and Hg.  Yg is F32 when wt is F32, else BF16.
+ *   - e4m3 scales are fp32: weights one per 128x128 block
+ *     ([slots][N/128][K/128]), grouped activations one per 1x128 group
+ *     ([rows][cols/128]).  Quantised value = code * scale.
+ *   - Weights are stored transposed with the reduced dimension contiguous:
+ *     W13 [P+S][2I][H] (rows 0..I-1 = gate W1^T, rows I..2I-1 = up W3^T),
+ *     W2 [P+S][H][I].  Slot s holds the weights of the logical expert
+ *     physical_to_logical[s] (a replica is a copy).
+ *   - Grouped buffers have `rows` rows: (P+S)*M_max (masked layout, row of
+ *     slot s rank r = s*M_max + r) or T*K + S*T (contiguous layout, row =
+ *     offsets[s] + r).  Rows of a slot hold its tokens in ascending token
+ *     order.  Rows at or past masked_m[s] are padding: no call writes them.
+ */
+#ifndef MOE_GB300_H
+#define MOE_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum moe_status {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,     /* a null pointer, a size out of range, an inconsistent problem */
+  MOE_ERR_UNSUPPORTED = -2, /* a valid problem this build does not run (dtype combination, alignment) */
+  MOE_ERR_CUDA = -3,        /* a CUDA runtime error at launch */
+  MOE_ERR_WORKSPACE = -4    /* workspace smaller than moe_workspace_bytes() */
+} moe_status;
+
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+
+typedef enum moe_layout { MOE_LAYOUT_MASKED = 0, MOE_LAYOUT_CONTIG = 1 } moe_layout;
+
+/* Bits of the device error flag. */
+#define MOE_FLAG_OVERFLOW 1   /* a slot received more than M_max rows (masked layout); extra rows not written, their row_of is -1 */
+#define MOE_FLAG_BAD_EXPERT 2 /* an expert id outside [0,E), or one token naming an expert twice */
+#define MOE_FLAG_BAD_MAP 4    /* a physical_to_logical entry outside [0,E), or a routed expert held by no slot */
+#define MOE_FLAG_TIMEOUT 8    /* a pipeline wait inside a GEMM kernel gave up; its outputs are incomplete */
+
+/* CUDA stream, ABI-compatible with cudaStream_t. */
+typedef struct CUstream_st* moe_stream_t;
+
+typedef struct moe_problem {
+  int32_t T;          /* tokens, >= 0 */
+  int32_t H;          /* hidden size */
+  int32_t I;          /* expert intermediate size */
+  int32_t E;          /* logical routed experts, 1..1024 */
+  int32_t K;          /* experts per token, 1..min(E, 32) */
+  int32_t P;          /* physical slots, >= E (== E without a replica map) */
+  int32_t M_max;      /* rows per slot of the masked layout; >= T when has_shared; unused for contiguous */
+  int32_t has_shared; /* 1 = one always-on shared expert in slot P, weight 1 */
+  int32_t act;        /* moe_dtype of x */
+  int32_t wt;         /* moe_dtype of the expert weights, Xg and Hg */
+  int32_t out;        /* moe_dtype of the layer output */
+  int32_t layout;     /* moe_layout of the grouped buffers */
+} moe_problem;
+
+/* Library version, (major << 16) | minor. */
+int32_t moe_version(void);
+
+/* A static string naming a status code. */
+const char* moe_status_string(int32_t status);
+
+/* Rows of the grouped buffers for this problem (see the conventions above). */
+int64_t moe_grouped_rows(const moe_problem* p);
+
+/* Workspace bytes one call sequence needs (the maximum over all calls).
+ * One workspace may serve every call of a layer as long as the calls are
+ * ordered on one stream.  Returns 0 for an invalid problem. */
+size_t moe_workspace_bytes(const moe_problem* p);
+
+/* Check a problem without touching the GPU: MOE_OK, MOE_ERR_INVALID or
+ * MOE_ERR_UNSUPPORTED. */
+moe_status moe_check_problem(const moe_problem* p);
+
+/* Step 1 (routing; "MoE inference and expert parallelism", routing section,
+ * Table 3-1).  For each token t: the K largest of the E logits, in descending
+ * order, ties to the lower expert index; weights
+ * w[t,k] = exp(l_k - l_max) / sum_j exp(l_j - l_max) over the chosen K
+ * (= softmax over all E renormalised over the K; fp32).
+ *   logits [T][E] fp32 (device, read), ids [T][K] int32 and w [T][K] fp32
+ *   (device, written).  One warp per token. */
+moe_status moe_route_topk(const moe_problem* p, const float* logits, int32_t* ids, float* w, moe_stream_t stream);
+
+/* Step 2 (dispatch; "Inference INFRA methodology (5)", section "DeepGEMM";
+ * "vLLM EPLB", section 1.2; "MoonEP", sections "Why dynamic routing is hard"
+ * and "Zero-copy and static buffer").
+ *   ids [T][K] int32: logical expert ids (from moe_route_topk).
+ *   x [T][H]: activations, dtype p->act.
+ *   phys_to_log [P] int32 or NULL: physical_to_logical_map.  With a map, a
+ *     record (t, k) of logical expert e goes to the (t mod c)-th slot holding
+ *     e, slots taken in ascending index, c = logical_replica_count[e]
+ *     (round-robin by token index).  Without one, slot = e and P must be E.
+ * Writes:
+ *   masked_m [P+S] int32: rows per slot (the shared slot holds T).
+ *   offsets [P+S+1] int32: exclusive prefix sum of masked_m.
+ *   row_of [T][K+S] int32: grouped row of record (t,k); column K is the
+ *     shared expert's row.  -1 for a record that was not placed (see err_flag).
+ *   src_of [rows] int32: token of each written row (padding rows untouched).
+ *   xg [rows][H], dtype p->wt: x[t] copied to its rows; for e4m3 each row is
+ *     quantised per 1x128 group: s = amax/448 (fp32 IEEE division, s = 1 for an
+ *     all-zero group), code = e4m3(x / s) nearest-even, saturating.
+ *   xg_scales [rows][H/128] fp32: the group scales (e4m3 only, else NULL).
+ *   err_flag: device int32, MOE_FLAG_* bits are OR-ed in (never cleared).
+ *   workspace: device scratch of moe_workspace_bytes(p) bytes. */
+moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, const int32_t* phys_to_log,
+                       int32_t* masked_m, int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg,
+                       float* xg_scales, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                       moe_stream_t stream);
+
+/* Step 3 (expert gate/up; "MoE inference and expert parallelism", routing
+ * section: SwiGLU with W1 = gate, W3 = up; "Inference INFRA methodology (5)",
+ * section "DeepGEMM": masked_m read on the device, no MMA for padding tiles,
+ * FP8 accumulated in FP32 once per 128-wide K block).
+ * For every slot s and row r < masked_m[s] (row index per the layout):
+ *   g = W1[s] . xg[row], u = W3[s] . xg[row], h = SiLU(g) * u
+ *   hg[row][0..I) = h, stored as p->wt (e4m3: 1x128 groups as in moe_permute,
+ *   scales in hg_scales [rows][I/128]; bf16: nearest-even; f32: as is).
+ *   xg_scales / w13_scales / hg_scales: e4m3 only, else NULL.
+ *   masked_m [P+S], offsets [P+S+1]: as written by moe_permute (device).
+ * bf16 / e4m3 run on the tcgen05 tensor cores and need H, I multiples of 128. */
+moe_status moe_grouped_swiglu_gemm(const moe_problem* p, const void* xg, const float* xg_scales, const void* w13,
+                                   const float* w13_scales, const int32_t* masked_m, const int32_t* offsets,
+                                   void* hg, float* hg_scales, int32_t* err_flag, void* workspace,
+                                   size_t workspace_bytes, moe_stream_t stream);
+
+/* Step 4 (expert down): yg[row][0..H) = W2[s] . hg[row] for every valid row,
+ * stored as fp32 (wt = F32) or bf16.  Same skipping and promotion as step 3. */
+moe_status moe_grouped_down_gemm(const moe_problem* p, const void* hg, const float* hg_scales, const void* w2,
+                                 const float* w2_scales, const int32_t* masked_m, const int32_t* offsets,
+                                 void* yg, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                                 moe_stream_t stream);
+
+/* Step 5 (combine; "MoE inference and expert parallelism", routing section:
+ * moe_sum / TopKWeightAndReduce, DeepSeek-V3 Eq. 12 for the shared expert):
+ *   out[t] = sum_{k<K} w[t,k] * yg[row_of[t,k]]  (+ yg[row_of[t,K]] if S),
+ * summed in fp32 in k order, then rounded once to p->out.  Records with
+ * row_of = -1 are skipped.  yg [rows][H] (F32 or BF16 per p->wt), row_of
+ * [T][K+S], w [T][K] fp32, out [T][H] (p->out). */
+moe_status moe_combine(const moe_problem* p, const void* yg, const int32_t* row_of, const float* w, void* out,
+                       moe_stream_t stream);
+
+/* Host helper ("vLLM EPLB", section 1.2): invert a physical_to_logical map.
+ * All pointers are HOST pointers.  p2l [P] in, l2p [E][R] out (slots of each
+ * logical expert in ascending order, padded with -1), rc [E] out.  Returns
+ * the largest replica count, or MOE_ERR_INVALID for an entry outside [0,E) or
+ * an expert with more than R replicas. */
+int32_t moe_eplb_invert(int32_t P, int32_t E, const int32_t* p2l, int32_t R, int32_t* l2p, int32_t* rc);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_GB300_H */

@@ -1,0 +1,835 @@
+// Steps 3 and 4: grouped per-expert GEMMs on the tcgen05 tensor cores.
+//
+// "Inference INFRA methodology (5)", section "DeepGEMM": the activations sit
+// in a static expert-grouped buffer and the real row count of each expert
+// (masked_m) lives in device memory; the kernel reads it at run time, so the
+// launch shape is fixed and CUDA-graph capturable, and a tile that would hold
+// only padding rows issues no MMA.  FP8 products are accumulated by the tensor
+// core over one 128-wide K block and promoted to an FP32 accumulator with the
+// weight-block and activation-group scales on the CUDA cores ("two-level
+// accumulation").  "MoE inference and expert parallelism", routing section:
+// the expert is SwiGLU with W1 = gate, W3 = up, W2 = down.
+//
+// Design (GB300, one CTA per SM, persistent):
+//   * Swap-AB: the weights fill the MMA's M = 128 side and the tokens of one
+//     expert (up to 128 per unit) its N side, so a decode expert with a
+//     handful of tokens still streams its weights once at full width, and N
+//     is rounded only to 16 (no MMA for padding past that).
+//   * A unit is (slot s, token chunk c of 128 rows, tile pair j, K split q).
+//     Gate/up: the pair is the gate tile rows [128j, 128j+128) and the up tile
+//     at rows I + 128j, sharing one B (token) tile.  Down: two consecutive
+//     128-row tiles of W2.  Units exist only for chunks with at least one real
+//     row: the kernel builds the unit list from masked_m on the device.
+//   * Warp 0: TMA producer (weights with an evict-first L2 hint; token tile
+//     with a box of 16/32/64/128 rows, the smallest that covers the chunk).
+//     Warp 1: tensor-memory allocator and the single MMA-issuing thread.
+//     Warps 2-9: epilogue, two warps per tensor-memory lane quarter, each
+//     owning 64 of the 128 token columns.
+//   * FP8: the MMA writes each 128-K block into one of two tensor-memory
+//     buffers; the epilogue reads it, scales by s_w * s_x and adds into
+//     registers while the MMA fills the other buffer.  BF16: the whole K range
+//     accumulates in tensor memory; the two buffers alternate between units.
+//   * Every wait is bounded in time; on expiry the CTA sets an abort flag,
+//     drains its copies and MMAs, frees tensor memory, reports
+//     MOE_FLAG_TIMEOUT and returns.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int BM = 128;                      // weight rows per tile (MMA M)
+constexpr int BN = 128;                      // tokens per unit (largest MMA N used)
+constexpr int ROW_BYTES = 128;               // K bytes per stage row (one 128-byte swizzle span)
+constexpr int TILE_A_BYTES = BM * ROW_BYTES;
+constexpr int TILE_B_BYTES = BN * ROW_BYTES;
+constexpr int STAGE_BYTES = 2 * TILE_A_BYTES + TILE_B_BYTES;
+constexpr int NUM_THREADS = 384;  // three warpgroups
+constexpr int EPI_THREADS = 256;  // warpgroups 1 and 2
+constexpr int EPI_WARP0 = 4;
+// Register split (setmaxnreg): warpgroup 0 (TMA + MMA) gives registers to the
+// two epilogue warpgroups, which hold 2 x 64 fp32 accumulators per thread.
+// 4*32*REGS_CTRL + 8*32*REGS_EPI must not exceed 384 * (registers at launch).
+constexpr int REGS_CTRL = 64;
+constexpr int REGS_EPI = 216;
+constexpr int REGS_NEEDED = 4 * 32 * REGS_CTRL + 8 * 32 * REGS_EPI;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t TIMEOUT_NS = 2000000000ull;
+
+struct TcParams {
+  int nslots, masked, M_max;
+  int kb_total;      // 128-byte K blocks of the reduction
+  int kb_per_split;  // K blocks per split
+  int ksplit;
+  int NA;            // weight rows per slot
+  int pairs;         // tile pairs per token chunk
+  int pair_stride;   // weight rows between pairs
+  int a1_off;        // row of the second tile of a pair relative to the first
+  int out_cols;      // columns of the output rows
+  int scale_cols;    // K / 128 (e4m3 scales per row of weights and activations)
+  int stages;
+  const int32_t* masked_m;
+  const int32_t* offsets;
+  const float* a_scales;  // weight block scales [slots * NA/128][K/128]
+  const float* b_scales;  // activation group scales [rows][K/128]
+  void* out;
+  float* out_scales;      // e4m3 gate/up output scales [rows][I/128]
+  float* part;            // split-K partial tiles
+  int32_t* counters;      // split-K arrival counters (zero between calls)
+  int32_t* err;
+  uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
+};
+
+struct Unit {
+  int s, c, j, q;
+  int nvalid;
+  int rowB, rowA0, rowA1;
+  int kb0, kb1;
+  bool a1;
+};
+
+__device__ __forceinline__ int slot_rows(const TcParams& p, int s) {
+  int m = __ldg(p.masked_m + s);
+  if (p.masked) m = min(m, p.M_max);
+  return max(m, 0);
+}
+
+template <int MODE>
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* prefix, int u) {
+  int lo = 0, hi = p.nslots;  // prefix[lo] <= u < prefix[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prefix[mid] <= u)
+      lo = mid;
+    else
+      hi = mid;
+  }
+  Unit U;
+  U.s = lo;
+  const int r = u - prefix[lo];
+  const int m = slot_rows(p, lo);
+  const int nch = (m + BN - 1) / BN;
+  U.q = r % p.ksplit;
+  const int rest = r / p.ksplit;
+  U.c = rest % nch;
+  U.j = rest / nch;
+  U.nvalid = min(BN, m - U.c * BN);
+  U.rowB = (p.masked ? lo * p.M_max : __ldg(p.offsets + lo)) + U.c * BN;
+  U.rowA0 = lo * p.NA + U.j * p.pair_stride;
+  U.rowA1 = U.rowA0 + p.a1_off;
+  U.a1 = (MODE == MODE_SWIGLU) ? true : (U.j * p.pair_stride + p.a1_off < p.NA);
+  U.kb0 = U.q * p.kb_per_split;
+  U.kb1 = min(p.kb_total, U.kb0 + p.kb_per_split);
+  return U;
+}
+
+template <typename T>
+__device__ __forceinline__ void store_bf16(T* base, size_t idx, float v) {
+  reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+}
+
+template <bool F8, int MODE>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
+                           const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
+                           const __grid_constant__ CUtensorMap tmB128, const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
+  float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [kb_per_split][BN] activation scales
+  float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [2][kb_per_split] weight scales
+  float* red = reinterpret_cast<float*>(smem + p.red_off);  // [2 halves][4 quarters][64] column maxima
+  int* prefix = reinterpret_cast<int*>(smem + p.pre_off);   // [nslots + 1] unit prefix
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  uint64_t* empty = full + p.stages;
+  uint64_t* tfull = empty + p.stages;  // [2]
+  uint64_t* tempty = tfull + 2;        // [2]
+  uint64_t* drain = tempty + 2;        // [1]
+  uint64_t* ebar = drain + 1;          // [1] all epilogue threads
+  uint64_t* hbar = ebar + 1;           // [2] the 128 epilogue threads of one column half
+  uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + p.misc_off);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
+  int* last_flag = reinterpret_cast<int*>(smem + p.misc_off + 8);
+
+  const int tid = threadIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int i = 0; i < p.stages; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&tfull[i], 1);
+      mbar_init(&tempty[i], EPI_THREADS);
+    }
+    mbar_init(drain, 1);
+    mbar_init(ebar, EPI_THREADS);
+    mbar_init(&hbar[0], 128);
+    mbar_init(&hbar[1], 128);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_base_smem, TMEM_COLS);
+    tmem_relinquish();
+  }
+  // unit counts per slot -> prefix
+  for (int s = tid; s < p.nslots; s += NUM_THREADS) {
+    const int nch = (slot_rows(p, s) + BN - 1) / BN;
+    prefix[s + 1] = nch * p.pairs * p.ksplit;
+  }
+  if (tid == 0) prefix[0] = 0;
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 0) {
+    int run = 0;
+    for (int base = 1; base <= p.nslots; base += 32) {
+      const int i = base + lane;
+      int v = (i <= p.nslots) ? prefix[i] : 0;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += n;
+      }
+      if (i <= p.nslots) prefix[i] = run + v;
+      run += __shfl_sync(0xffffffffu, v, 31);
+    }
+  }
+  __syncthreads();
+  tc_fence_after_sync();
+  const uint32_t tmem_base = *tmem_base_smem;
+  const int total = prefix[p.nslots];
+  if (warp < EPI_WARP0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      tma_prefetch_map(&tmA);
+      tma_prefetch_map(&tmB16);
+      tma_prefetch_map(&tmB32);
+      tma_prefetch_map(&tmB64);
+      tma_prefetch_map(&tmB128);
+      const uint64_t pol = policy_evict_first();
+      const int kb_elems = F8 ? ROW_BYTES : ROW_BYTES / 2;
+      int stage = 0;
+      uint32_t phase = 0;
+      long issued = 0;
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        const Unit U = decode_unit<MODE>(p, prefix, u);
+        const CUtensorMap* mb;
+        int box;
+        if (U.nvalid <= 16) {
+          mb = &tmB16;
+          box = 16;
+        } else if (U.nvalid <= 32) {
+          mb = &tmB32;
+          box = 32;
+        } else if (U.nvalid <= 64) {
+          mb = &tmB64;
+          box = 64;
+        } else {
+          mb = &tmB128;
+          box = 128;
+        }
+        const uint32_t bytes = TILE_A_BYTES * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT_NS)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sA0 = smem + (size_t)stage * STAGE_BYTES;
+          mbar_arrive_expect_tx(&full[stage], bytes);
+          const int x = kb * kb_elems;
+          tma_load_2d_hint(sA0, &tmA, &full[stage], x, U.rowA0, pol);
+          if (U.a1) tma_load_2d_hint(sA0 + TILE_A_BYTES, &tmA, &full[stage], x, U.rowA1, pol);
+          tma_load_2d(sA0 + 2 * TILE_A_BYTES, mb, &full[stage], x, U.rowB);
+          ++issued;
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+      }
+      if (!ok) {
+        // let the copies already in flight land before the CTA's shared memory is released
+        const long first = issued > p.stages ? issued - p.stages : 0;
+        for (long i = first; i < issued; ++i) {
+          const int st = (int)(i % p.stages);
+          const uint32_t ph = (uint32_t)((i / p.stages) & 1);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(&full[st], ph) && global_timer_ns() - t0 < TIMEOUT_NS) {
+          }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      uint32_t acc_it = 0;
+      bool ok = true;
+      bool any = false;
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        const Unit U = decode_unit<MODE>(p, prefix, u);
+        const int N = (U.nvalid + 15) & ~15;
+        const uint32_t idesc = mma_idesc<F8>(BM, N);
+        uint32_t b = 0;
+        if constexpr (!F8) {
+          b = acc_it & 1u;
+          if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+        }
+        for (int kb = U.kb0; kb < U.kb1; ++kb) {
+          if constexpr (F8) {
+            b = acc_it & 1u;
+            if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!mbar_wait(&full[stage], phase, abort_flag, TIMEOUT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const uint32_t a0 = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+          const uint64_t da0 = smem_desc_sw128(a0);
+          const uint64_t da1 = smem_desc_sw128(a0 + TILE_A_BYTES);
+          const uint64_t db = smem_desc_sw128(a0 + 2 * TILE_A_BYTES);
+          const uint32_t d0 = tmem_base + b * 256u;
+          const uint32_t d1 = d0 + 128u;
+#pragma unroll
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint32_t acc = F8 ? (ks > 0) : (kb > U.kb0 || ks > 0);
+            tc_mma<F8>(d0, da0 + 2 * ks, db + 2 * ks, idesc, acc);
+            if (U.a1) tc_mma<F8>(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
+          }
+          any = true;
+          tc_commit(&empty[stage]);
+          if constexpr (F8) {
+            tc_commit(&tfull[b]);
+            ++acc_it;
+          }
+          if (++stage == p.stages) {
+            stage = 0;
+            phase ^= 1u;
+          }
+        }
+        if constexpr (!F8) {
+          if (ok) {
+            tc_commit(&tfull[b]);
+            ++acc_it;
+          }
+        }
+      }
+      if (!ok && any) {
+        // all MMAs issued by this thread must finish before tensor memory is freed
+        tc_commit(drain);
+        const uint64_t t0 = global_timer_ns();
+        while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < TIMEOUT_NS) {
+        }
+      }
+    }
+  }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
+    // ------------------------------------------------------------ epilogue
+    const int etid = tid - EPI_WARP0 * 32;
+    const int ew = warp - EPI_WARP0;
+    const int quarter = warp & 3;  // tensor-memory lane quarter this warp may access
+    const int half = ew >> 2;      // token columns [64*half, 64*half + 64) (warpgroup 1 or 2)
+    const int lrow = quarter * 32 + lane;
+    const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
+    uint32_t acc_it = 0;
+    uint32_t ephase = 0, hphase = 0;
+    bool ok = true;
+    const size_t oc = (size_t)p.out_cols;
+    // bounded barriers among the epilogue threads (a plain bar.sync could not give up)
+    auto epi_sync = [&]() {
+      mbar_arrive(ebar);
+      const bool r = mbar_wait(ebar, ephase, abort_flag, TIMEOUT_NS);
+      ephase ^= 1u;
+      return r;
+    };
+    auto half_sync = [&](int h) {
+      mbar_arrive(&hbar[h]);
+      const bool r = mbar_wait(&hbar[h], hphase, abort_flag, TIMEOUT_NS);
+      hphase ^= 1u;
+      return r;
+    };
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+      const Unit U = decode_unit<MODE>(p, prefix, u);
+      const int c_lo = half * 64;
+      const int ncols = max(0, min(64, U.nvalid - c_lo));
+      const int nch = (ncols + 15) >> 4;
+      const int nkb = U.kb1 - U.kb0;
+      const bool split = p.ksplit > 1;
+      // output column of this lane for tile 0 / tile 1 of the pair
+      const int col0 = (MODE == MODE_SWIGLU) ? U.j * BM + lrow : U.j * p.pair_stride + lrow;
+      const int col1 = col0 + BM;
+
+      // writes the final values of token column c (0..BN) for this lane
+      auto finish = [&](int c, float v0, float v1) {
+        const size_t row = (size_t)(U.rowB + c);
+        if constexpr (MODE == MODE_SWIGLU) {
+          const float h = silu(v0) * v1;
+          if constexpr (!F8) {
+            store_bf16(p.out, row * oc + col0, h);
+          } else {
+            (void)h;  // e4m3 output is finished group-wise below
+          }
+        } else {
+          store_bf16(p.out, row * oc + col0, v0);
+          if (U.a1) store_bf16(p.out, row * oc + col1, v1);
+        }
+      };
+
+      if constexpr (F8) {
+        float acc0[64], acc1[64];
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          acc0[i] = 0.0f;
+          acc1[i] = 0.0f;
+        }
+        if (!epi_sync()) break;  // readers of the previous unit's scales are done
+        {
+          const int n = U.nvalid;
+          for (int i = etid; i < n * nkb; i += EPI_THREADS) {
+            const int c = i / nkb, k = i - c * nkb;
+            sx[k * BN + c] = __ldg(p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + U.kb0 + k);
+          }
+          const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
+          for (int k = etid; k < nkb; k += EPI_THREADS) {
+            sw[k] = __ldg(p.a_scales + (size_t)ra0 * p.scale_cols + U.kb0 + k);
+            sw[p.kb_per_split + k] = U.a1 ? __ldg(p.a_scales + (size_t)ra1 * p.scale_cols + U.kb0 + k) : 0.0f;
+          }
+        }
+        if (!epi_sync()) break;
+        for (int k = 0; k < nkb; ++k) {
+          const uint32_t b = acc_it & 1u;
+          if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after_sync();
+          const float s0 = sw[k], s1 = sw[p.kb_per_split + k];
+          const float* sxk = sx + k * BN + c_lo;
+#pragma unroll
+          for (int ch = 0; ch < 4; ++ch) {
+            if (ch < nch) {
+              float v0[16], v1[16];
+              const uint32_t col = b * 256u + (uint32_t)(c_lo + ch * 16);
+              tmem_ld16x2(t_lane + col, t_lane + col + 128u, v0, v1);
+#pragma unroll
+              for (int i = 0; i < 16; ++i) {
+                const float xs = sxk[ch * 16 + i];
+                acc0[ch * 16 + i] = fmaf(v0[i], s0 * xs, acc0[ch * 16 + i]);
+                acc1[ch * 16 + i] = fmaf(v1[i], s1 * xs, acc1[ch * 16 + i]);
+              }
+            }
+          }
+          tc_fence_before_sync();
+          mbar_arrive(&tempty[b]);
+          ++acc_it;
+        }
+        if (!ok) break;
+
+        if (split) {
+          // publish this split's partial tile, the last arriving split finishes it
+          const size_t tile = (size_t)(u / p.ksplit);
+          float* mine = p.part + ((tile * p.ksplit + U.q) * 2) * (size_t)BN * BM;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (i < ncols) {
+              mine[(size_t)(c_lo + i) * BM + lrow] = acc0[i];
+              mine[(size_t)(BN + c_lo + i) * BM + lrow] = acc1[i];
+            }
+          }
+          __threadfence();
+          if (!epi_sync()) break;
+          if (etid == 0) *last_flag = (atomicAdd(p.counters + tile, 1) == p.ksplit - 1);
+          if (!epi_sync()) break;
+          if (!*last_flag) continue;
+          __threadfence();
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (i < ncols) {
+              float v0 = 0.0f, v1 = 0.0f;
+              for (int q = 0; q < p.ksplit; ++q) {
+                const float* pq = p.part + ((tile * p.ksplit + q) * 2) * (size_t)BN * BM;
+                v0 += __ldcg(pq + (size_t)(c_lo + i) * BM + lrow);
+                v1 += __ldcg(pq + (size_t)(BN + c_lo + i) * BM + lrow);
+              }
+              acc0[i] = v0;
+              acc1[i] = v1;
+            }
+          }
+          if (etid == 0) p.counters[tile] = 0;
+        }
+
+        if constexpr (MODE == MODE_SWIGLU) {
+          // h = silu(g) * u, then e4m3 per 1x128 group: the group is this tile's 128 rows
+          float* redh = red + half * 4 * 64;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (i < ncols) {
+              const float h = silu(acc0[i]) * acc1[i];
+              acc0[i] = h;
+              float a = fabsf(h);
+#pragma unroll
+              for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
+              if (lane == 0) redh[quarter * 64 + i] = a;
+            }
+          }
+          if (!half_sync(half)) break;
+          uint8_t* hq = static_cast<uint8_t*>(p.out);
+          const int G = p.out_cols / 128;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (i < ncols) {
+              const float amax =
+                  fmaxf(fmaxf(redh[i], redh[64 + i]), fmaxf(redh[128 + i], redh[192 + i]));
+              const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+              const size_t row = (size_t)(U.rowB + c_lo + i);
+              const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(__fdiv_rn(acc0[i], sc), __NV_SATFINITE, __NV_E4M3);
+              hq[row * oc + col0] = code;
+              if (quarter == 0 && lane == 0) p.out_scales[row * G + U.j] = sc;
+            }
+          }
+          if (!half_sync(half)) break;  // the maxima are read before the next unit writes them
+        } else {
+#pragma unroll
+          for (int i = 0; i < 64; ++i)
+            if (i < ncols) finish(c_lo + i, acc0[i], acc1[i]);
+        }
+      } else {
+        // BF16: the accumulator of the whole K range (or this split of it) is in tensor memory
+        const uint32_t b = acc_it & 1u;
+        if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after_sync();
+        const size_t tile = (size_t)(u / p.ksplit);
+        float* mine = split ? p.part + ((tile * p.ksplit + U.q) * 2) * (size_t)BN * BM : nullptr;
+#pragma unroll
+        for (int ch = 0; ch < 4; ++ch) {
+          if (ch < nch) {
+            float v0[16], v1[16];
+            const uint32_t col = b * 256u + (uint32_t)(c_lo + ch * 16);
+            tmem_ld16x2(t_lane + col, t_lane + col + 128u, v0, v1);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int c = c_lo + ch * 16 + i;
+              if (c < U.nvalid) {
+                if (split) {
+                  mine[(size_t)c * BM + lrow] = v0[i];
+                  mine[(size_t)(BN + c) * BM + lrow] = v1[i];
+                } else {
+                  finish(c, v0[i], v1[i]);
+                }
+              }
+            }
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&tempty[b]);
+        ++acc_it;
+        if (split) {
+          __threadfence();
+          if (!epi_sync()) break;
+          if (etid == 0) *last_flag = (atomicAdd(p.counters + tile, 1) == p.ksplit - 1);
+          if (!epi_sync()) break;
+          if (*last_flag) {
+            __threadfence();
+            for (int i = 0; i < ncols; ++i) {
+              float v0 = 0.0f, v1 = 0.0f;
+              for (int q = 0; q < p.ksplit; ++q) {
+                const float* pq = p.part + ((tile * p.ksplit + q) * 2) * (size_t)BN * BM;
+                v0 += __ldcg(pq + (size_t)(c_lo + i) * BM + lrow);
+                v1 += __ldcg(pq + (size_t)(BN + c_lo + i) * BM + lrow);
+              }
+              finish(c_lo + i, v0, v1);
+            }
+            if (etid == 0) p.counters[tile] = 0;
+          }
+          if (!epi_sync()) break;  // last_flag is read before the next unit overwrites it
+        }
+      }
+    }
+  }
+
+  tc_fence_before_sync();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after_sync();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+  if (tid == 0 && *abort_flag) atomicOr(p.err, MOE_FLAG_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------
+// Host side
+// ---------------------------------------------------------------------------
+
+struct Plan {
+  int ksplit, kb_per_split, kb_total, stages, nslots, pairs;
+  size_t smem;
+  uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
+  size_t part_bytes, counter_bytes;
+};
+
+Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
+  Plan pl{};
+  const bool f8 = p.wt == MOE_E4M3;
+  const int esz = f8 ? 1 : 2;
+  const int K = (mode == MODE_SWIGLU) ? p.H : p.I;
+  const int NA = (mode == MODE_SWIGLU) ? 2 * p.I : p.H;
+  pl.kb_total = K * esz / ROW_BYTES;
+  pl.nslots = p.P + p.has_shared;
+  pl.pairs = (mode == MODE_SWIGLU) ? p.I / BM : (NA + 2 * BM - 1) / (2 * BM);
+  // upper bound of the token chunks over all slots
+  long chunks;
+  if (p.layout == MOE_LAYOUT_MASKED) {
+    chunks = (long)pl.nslots * ((p.M_max + BN - 1) / BN);
+  } else {
+    const long rows = (long)p.T * p.K + (long)p.has_shared * p.T;
+    chunks = std::min<long>((long)pl.nslots * ((p.T + BN - 1) / BN), pl.nslots + rows / BN);
+  }
+  const long tiles = chunks * pl.pairs;
+  pl.ksplit = 1;
+  if (mode == MODE_DOWN && tiles > 0 && tiles < 3L * sm_count) {
+    // split K so the unit count fills whole waves; keep >= 4 K blocks per split
+    double best = 0.0;
+    for (int ks = 1; ks <= 16 && pl.kb_total / ks >= 4; ++ks) {
+      const double waves = (double)(tiles * ks) / sm_count;
+      const double eff = waves / std::ceil(waves);
+      if (eff > best + 0.02) {
+        best = eff;
+        pl.ksplit = ks;
+      }
+      if (waves >= 2.0 && eff >= 0.9) {
+        pl.ksplit = ks;
+        break;
+      }
+    }
+  }
+  pl.kb_per_split = (pl.kb_total + pl.ksplit - 1) / pl.ksplit;
+  pl.ksplit = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  // shared memory carve (offsets relative to the 1024-aligned base)
+  size_t extra = 0;
+  auto carve = [&](size_t bytes, size_t align) {
+    extra = align_up(extra, align);
+    const size_t off = extra;
+    extra += bytes;
+    return off;
+  };
+  // reserve stage space first, assume the maximum; offsets of the rest follow the stages
+  const size_t sx_b = f8 ? (size_t)pl.kb_per_split * BN * 4 : 0;
+  const size_t sw_b = f8 ? (size_t)2 * pl.kb_per_split * 4 : 0;
+  const size_t red_b = (f8 && mode == MODE_SWIGLU) ? 2 * 4 * 64 * 4 : 0;
+  const size_t pre_b = (size_t)(pl.nslots + 1) * 4;
+  for (int st = 6; st >= 2; --st) {
+    extra = (size_t)st * STAGE_BYTES;
+    pl.sx_off = (uint32_t)carve(sx_b, 16);
+    pl.sw_off = (uint32_t)carve(sw_b, 16);
+    pl.red_off = (uint32_t)carve(red_b, 16);
+    pl.pre_off = (uint32_t)carve(pre_b, 16);
+    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 8) * 8, 8);
+    pl.misc_off = (uint32_t)carve(16, 16);
+    const size_t total = extra + 1024;
+    if ((int)total <= smem_cap) {
+      pl.stages = st;
+      pl.smem = total;
+      break;
+    }
+  }
+  pl.part_bytes = pl.ksplit > 1 ? (size_t)tiles * pl.ksplit * 2 * BN * BM * 4 : 0;
+  pl.counter_bytes = pl.ksplit > 1 ? (size_t)tiles * 4 : 0;
+  return pl;
+}
+
+template <bool F8, int MODE>
+int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float* act_scales, const void* w,
+              const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
+              int32_t* err, void* ws, cudaStream_t st) {
+  const DeviceInfo& di = device_info();
+  static bool attr_set[2][2][64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  auto kern = grouped_gemm_tc_kernel<F8, MODE>;
+  if (dev < 64 && !attr_set[F8][MODE][dev]) {
+    // the register split above must fit in what the launch provides, or setmaxnreg.inc would wait forever
+    cudaFuncAttributes fa{};
+    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return MOE_ERR_CUDA;
+    if (fa.numRegs * NUM_THREADS < REGS_NEEDED) return MOE_ERR_UNSUPPORTED;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    attr_set[F8][MODE][dev] = true;
+  }
+  const int esz = F8 ? 1 : 2;
+  const CUtensorMapDataType dt = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int K = (MODE == MODE_SWIGLU) ? p.H : p.I;
+  const int NA = (MODE == MODE_SWIGLU) ? 2 * p.I : p.H;
+  const uint64_t rowsA = (uint64_t)pl.nslots * NA;
+  const uint64_t rowsB = (uint64_t)grouped_rows(p);
+  const uint32_t box_k = ROW_BYTES / esz;
+  CUtensorMap tA, tB[4];
+  if (encode_tensor_map(&tA, dt, K, rowsA, (uint64_t)K * esz, box_k, BM, w) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  const int boxes[4] = {16, 32, 64, 128};
+  for (int i = 0; i < 4; ++i)
+    if (encode_tensor_map(&tB[i], dt, K, rowsB, (uint64_t)K * esz, box_k, boxes[i], act) != CUDA_SUCCESS)
+      return MOE_ERR_CUDA;
+
+  TcParams prm{};
+  prm.nslots = pl.nslots;
+  prm.masked = p.layout == MOE_LAYOUT_MASKED;
+  prm.M_max = p.M_max;
+  prm.kb_total = pl.kb_total;
+  prm.kb_per_split = pl.kb_per_split;
+  prm.ksplit = pl.ksplit;
+  prm.NA = NA;
+  prm.pairs = pl.pairs;
+  prm.pair_stride = (MODE == MODE_SWIGLU) ? BM : 2 * BM;
+  prm.a1_off = (MODE == MODE_SWIGLU) ? p.I : BM;
+  prm.out_cols = (MODE == MODE_SWIGLU) ? p.I : p.H;
+  prm.scale_cols = K / 128;
+  prm.stages = pl.stages;
+  prm.masked_m = masked_m;
+  prm.offsets = offsets;
+  prm.a_scales = w_scales;
+  prm.b_scales = act_scales;
+  prm.out = out;
+  prm.out_scales = out_scales;
+  prm.err = err;
+  prm.sx_off = pl.sx_off;
+  prm.sw_off = pl.sw_off;
+  prm.red_off = pl.red_off;
+  prm.pre_off = pl.pre_off;
+  prm.bar_off = pl.bar_off;
+  prm.misc_off = pl.misc_off;
+  if (pl.ksplit > 1) {
+    char* base = static_cast<char*>(ws);
+    prm.counters = reinterpret_cast<int32_t*>(base);
+    prm.part = reinterpret_cast<float*>(base + align_up(pl.counter_bytes, 256));
+    if (cudaMemsetAsync(prm.counters, 0, pl.counter_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  kern<<<di.sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], prm);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+// ---------------------------------------------------------------------------
+// fp32 path on the CUDA cores (small fp32 problems; the tensor-core path
+// covers bf16 and e4m3).  One warp per output column, lanes across K.
+// ---------------------------------------------------------------------------
+
+template <int MODE>
+__global__ void __launch_bounds__(256) grouped_gemm_f32_kernel(const float* __restrict__ act,
+                                                               const float* __restrict__ w,
+                                                               const int32_t* __restrict__ masked_m,
+                                                               const int32_t* __restrict__ offsets, float* __restrict__ out,
+                                                               int nslots, int masked, int M_max, long rows_total,
+                                                               int K, int NA, int out_cols, int I) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n = blockIdx.x * 8 + warp;  // output column
+  if (n >= out_cols) return;
+  const long r0 = (long)blockIdx.y * 8;
+  for (long R = r0; R < r0 + 8 && R < rows_total; ++R) {
+    int s;
+    if (masked) {
+      s = (int)(R / M_max);
+      const int r = (int)(R - (long)s * M_max);
+      if (r >= min(masked_m[s], M_max)) continue;  // padding row: nothing to compute
+    } else {
+      if (R >= offsets[nslots]) continue;
+      int lo = 0, hi = nslots;  // offsets[lo] <= R < offsets[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (offsets[mid] <= R)
+          lo = mid;
+        else
+          hi = mid;
+      }
+      s = lo;
+    }
+    const float* x = act + R * K;
+    const float* w0 = w + ((size_t)s * NA + n) * K;
+    float a0 = 0.0f, a1 = 0.0f;
+    if (MODE == MODE_SWIGLU) {
+      const float* w1 = w0 + (size_t)I * K;
+      for (int k = lane; k < K; k += 32) {
+        a0 = fmaf(w0[k], x[k], a0);
+        a1 = fmaf(w1[k], x[k], a1);
+      }
+    } else {
+      for (int k = lane; k < K; k += 32) a0 = fmaf(w0[k], x[k], a0);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      a0 += __shfl_xor_sync(0xffffffffu, a0, off);
+      a1 += __shfl_xor_sync(0xffffffffu, a1, off);
+    }
+    if (lane == 0) out[R * out_cols + n] = (MODE == MODE_SWIGLU) ? a0 / (1.0f + expf(-a0)) * a1 : a0;
+  }
+}
+
+}  // namespace
+
+size_t gemm_workspace_bytes(const moe_problem& p) {
+  if (p.wt == MOE_F32) return 0;
+  // Split-K state depends on the SM count; size it for the largest plausible GPU (up to 256 SMs).
+  size_t best = 0;
+  for (int mode = 0; mode < 2; ++mode) {
+    for (int sms : {132, 148, 152, 160, 170, 188, 256}) {
+      const Plan pl = make_plan(p, mode, sms, 232448);
+      best = std::max(best, align_up(pl.counter_bytes, 256) + pl.part_bytes);
+    }
+  }
+  return best;
+}
+
+int launch_gemm(const moe_problem& p, int mode, const void* act, const float* act_scales, const void* w,
+                const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
+                int32_t* err, void* ws, cudaStream_t st) {
+  const int nslots = p.P + p.has_shared;
+  if (p.wt == MOE_F32) {
+    const int K = (mode == MODE_SWIGLU) ? p.H : p.I;
+    const int NA = (mode == MODE_SWIGLU) ? 2 * p.I : p.H;
+    const int out_cols = (mode == MODE_SWIGLU) ? p.I : p.H;
+    const long rows = (long)grouped_rows(p);
+    if (rows == 0) return MOE_OK;
+    const dim3 grid((out_cols + 7) / 8, (unsigned)((rows + 7) / 8));
+    if (mode == MODE_SWIGLU)
+      grouped_gemm_f32_kernel<MODE_SWIGLU><<<grid, 256, 0, st>>>(
+          (const float*)act, (const float*)w, masked_m, offsets, (float*)out, nslots,
+          p.layout == MOE_LAYOUT_MASKED, p.M_max, rows, K, NA, out_cols, p.I);
+    else
+      grouped_gemm_f32_kernel<MODE_DOWN><<<grid, 256, 0, st>>>(
+          (const float*)act, (const float*)w, masked_m, offsets, (float*)out, nslots,
+          p.layout == MOE_LAYOUT_MASKED, p.M_max, rows, K, NA, out_cols, p.I);
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  const DeviceInfo& di = device_info();
+  const Plan pl = make_plan(p, mode, di.sm_count, di.max_smem_optin);
+  if (pl.stages == 0) return MOE_ERR_UNSUPPORTED;
+  const bool f8 = p.wt == MOE_E4M3;
+  if (f8 && mode == MODE_SWIGLU)
+    return launch_tc<true, MODE_SWIGLU>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales,
+                                        err, ws, st);
+  if (f8)
+    return launch_tc<true, MODE_DOWN>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err,
+                                      ws, st);
+  if (mode == MODE_SWIGLU)
+    return launch_tc<false, MODE_SWIGLU>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales,
+                                         err, ws, st);
+  return launch_tc<false, MODE_DOWN>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err,
+                                     ws, st);
+}
+
+}  // namespace moe

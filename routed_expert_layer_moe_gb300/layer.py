@@ -1,0 +1,80 @@
+"""The five calls of the forward pass chained over caller-owned device buffers.
+
+PyTorch provides device memory and the stream; each step runs in the
+library's kernels.  Buffers are allocated once (static shapes), so a forward
+call is graph-capturable after a first eager call."""
+from __future__ import annotations
+
+import torch
+
+from . import _lib as L
+
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+
+
+class MoeLayer:
+    """Buffers and calls for one problem.  Weights are slot-indexed tensors on the
+    device: w13 [P+S, 2I, H], w2 [P+S, H, I] (e4m3: uint8 codes with fp32 block
+    scales w13_s [P+S, 2I/128, H/128], w2_s [P+S, H/128, I/128])."""
+
+    def __init__(self, problem: L.Problem, act: str, wt: str, out: str, w13, w2, w13_s=None, w2_s=None,
+                 phys_to_log=None, device="cuda"):
+        self.p = problem
+        self.act, self.wt, self.out_dt = act, wt, out
+        st = L.moe_check_problem(problem)
+        if st != L.MOE_OK:
+            raise L.MoeError(st, "problem")
+        p = problem
+        dev = torch.device(device)
+        self.w13, self.w2, self.w13_s, self.w2_s = w13, w2, w13_s, w2_s
+        self.p2l = phys_to_log
+        S = p.has_shared
+        rows = L.moe_grouped_rows(p)
+        self.rows = rows
+        i32 = dict(dtype=torch.int32, device=dev)
+        self.ids = torch.empty((p.T, p.K), **i32)
+        self.w = torch.empty((p.T, p.K), dtype=torch.float32, device=dev)
+        self.masked_m = torch.empty(p.P + S, **i32)
+        self.offsets = torch.empty(p.P + S + 1, **i32)
+        self.row_of = torch.empty((p.T, p.K + S), **i32)
+        self.src_of = torch.full((rows,), -1, **i32)
+        gd = TORCH_DTYPE[wt]
+        yd = torch.float32 if wt == "f32" else torch.bfloat16
+        self.xg = torch.empty((rows, p.H), dtype=gd, device=dev)
+        self.hg = torch.empty((rows, p.I), dtype=gd, device=dev)
+        self.yg = torch.empty((rows, p.H), dtype=yd, device=dev)
+        f8 = wt == "e4m3"
+        self.xg_s = torch.empty((rows, p.H // 128), dtype=torch.float32, device=dev) if f8 else None
+        self.hg_s = torch.empty((rows, p.I // 128), dtype=torch.float32, device=dev) if f8 else None
+        self.out = torch.empty((p.T, p.H), dtype=TORCH_DTYPE[out], device=dev)
+        self.err = torch.zeros(1, **i32)
+        nbytes = max(L.moe_workspace_bytes(p), 256)
+        self.ws = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+
+    # -- the steps --------------------------------------------------------------
+    def route(self, logits, stream=None):
+        L.moe_route_topk(self.p, logits, self.ids, self.w, stream)
+
+    def permute(self, x, stream=None):
+        L.moe_permute(self.p, self.ids, x, self.p2l, self.masked_m, self.offsets, self.row_of, self.src_of,
+                      self.xg, self.xg_s, self.err, self.ws, stream)
+
+    def swiglu(self, stream=None):
+        L.moe_grouped_swiglu_gemm(self.p, self.xg, self.xg_s, self.w13, self.w13_s, self.masked_m, self.offsets,
+                                  self.hg, self.hg_s, self.err, self.ws, stream)
+
+    def down(self, stream=None):
+        L.moe_grouped_down_gemm(self.p, self.hg, self.hg_s, self.w2, self.w2_s, self.masked_m, self.offsets,
+                                self.yg, self.err, self.ws, stream)
+
+    def combine(self, stream=None):
+        L.moe_combine(self.p, self.yg, self.row_of, self.w, self.out, stream)
+
+    def forward(self, x, logits, stream=None):
+        """route -> permute -> gate/up -> down -> combine; returns self.out."""
+        self.route(logits, stream)
+        self.permute(x, stream)
+        self.swiglu(stream)
+        self.down(stream)
+        self.combine(stream)
+        return self.out

@@ -1,0 +1,94 @@
+"""The C ABI on the host: the library loads, exports every symbol include/moe.h
+declares, and rejects bad arguments before touching the GPU."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+
+import oracle
+import routed_expert_layer_moe_gb300 as moe
+from routed_expert_layer_moe_gb300 import build as moe_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    moe_build.build()
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_exports_every_declared_symbol():
+    L = moe.lib()
+    declared = header_functions()
+    assert set(declared) == set(moe.EXPORTS)
+    for name in declared:
+        assert hasattr(L, name), name
+    assert moe.moe_version() >> 16 == 1
+
+
+def test_problem_checks_without_gpu():
+    ok = moe.Problem.make(T=32, H=4096, I=14336, E=8, K=2, M_max=32)
+    assert moe.moe_check_problem(ok) == moe.MOE_OK
+    assert moe.moe_grouped_rows(ok) == 8 * 32
+    assert moe.moe_workspace_bytes(ok) > 0
+    bad = [
+        dict(T=-1), dict(K=0), dict(K=9), dict(E=0), dict(P=7), dict(M_max=0), dict(E=2000, P=2000),
+        dict(has_shared=1, M_max=16),
+    ]
+    for b in bad:
+        kw = dict(T=32, H=4096, I=14336, E=8, K=2, M_max=32)
+        kw.update(b)
+        assert moe.moe_check_problem(moe.Problem.make(**kw)) == moe.MOE_ERR_INVALID, b
+    # valid shapes this build does not run
+    assert moe.moe_check_problem(moe.Problem.make(T=4, H=100, I=128, E=8, K=2, M_max=4)) == moe.MOE_ERR_UNSUPPORTED
+    assert moe.moe_check_problem(
+        moe.Problem.make(T=4, H=128, I=128, E=8, K=2, M_max=4, act="f32", wt="bf16", out="f32")) == \
+        moe.MOE_ERR_UNSUPPORTED
+
+
+def test_null_pointers_rejected_before_launch():
+    L = moe.lib()
+    p = moe.Problem.make(T=4, H=128, I=128, E=8, K=2, M_max=4)
+    r = L.moe_route_topk(ctypes.byref(p), None, None, None, None)
+    assert r == moe.MOE_ERR_INVALID
+    r = L.moe_combine(ctypes.byref(p), None, None, None, None, None)
+    assert r == moe.MOE_ERR_INVALID
+    r = L.moe_permute(ctypes.byref(p), *([None] * 11), 0, None)
+    assert r == moe.MOE_ERR_INVALID
+    r = L.moe_grouped_swiglu_gemm(ctypes.byref(p), *([None] * 10), 0, None)
+    assert r == moe.MOE_ERR_INVALID
+    r = L.moe_grouped_down_gemm(ctypes.byref(p), *([None] * 9), 0, None)
+    assert r == moe.MOE_ERR_INVALID
+    # empty batch: nothing to route
+    p0 = moe.Problem.make(T=0, H=128, I=128, E=8, K=2, M_max=4)
+    assert L.moe_route_topk(ctypes.byref(p0), None, None, None, None) == moe.MOE_OK
+
+
+def test_workspace_too_small_rejected():
+    L = moe.lib()
+    p = moe.Problem.make(T=4, H=128, I=128, E=8, K=2, M_max=4)
+    fake = ctypes.c_void_p(256)  # never dereferenced: the size check comes first
+    r = L.moe_permute(ctypes.byref(p), fake, fake, None, fake, fake, fake, fake, fake, None, fake, fake, 1, None)
+    assert r == moe.MOE_ERR_WORKSPACE
+
+
+def test_host_eplb_invert_matches_oracle():
+    rng = np.random.default_rng(0)
+    for _ in range(50):
+        E = int(rng.integers(1, 9))
+        P = E + int(rng.integers(0, 5))
+        p2l = np.concatenate([np.arange(E), rng.integers(0, E, P - E)]).astype(np.int32)
+        rng.shuffle(p2l)
+        l2p, rc, r = moe.moe_eplb_invert(p2l, E, P)
+        ol2p, orc, oref = oracle.eplb_invert(p2l, E, P)
+        assert r == oref and (rc == orc).all() and (l2p[:, :r] == ol2p[:, :r]).all()
+    with pytest.raises(moe.MoeError):
+        moe.moe_eplb_invert([0, 5], 2, 2)

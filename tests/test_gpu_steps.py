@@ -1,0 +1,281 @@
+"""Each C-ABI call on the GPU against the fp64 oracle, on the reduced workloads.
+
+Integer outputs (ids, counts, offsets, row maps, quantised activations) must be
+bit-exact; values within max|err|/max|ref| of 1e-2 (bf16), 3e-2 (e4m3) or 1e-4
+(fp32).  Inputs of each call come from the generator or the oracle, never from
+another GPU call."""
+import numpy as np
+import pytest
+import torch
+
+import moe_inputs as mi
+import oracle
+import routed_expert_layer_moe_gb300 as moe
+from cases import SMALL
+from gpu_util import TOL, Workload, real, rel_err, to_dev, to_host
+
+pytestmark = pytest.mark.gpu
+
+NAMES = list(SMALL)
+SENT_I32 = -7
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    from routed_expert_layer_moe_gb300 import build
+    build.build()
+    torch.cuda.init()
+
+
+@pytest.fixture(scope="module")
+def workloads():
+    return {n: Workload(SMALL[n]) for n in NAMES}
+
+
+def oracle_layout(wl):
+    lay = oracle.layout(wl.cfg, wl.ids, wl.p2l)
+    assert lay["status"] == 0
+    return lay
+
+
+# ---- a1 route -----------------------------------------------------------------
+
+@pytest.mark.parametrize("name", NAMES)
+def test_route(workloads, name):
+    wl = workloads[name]
+    L = wl.layer()
+    L.route(to_dev(wl.logits))
+    torch.cuda.synchronize()
+    assert (to_host(L.ids) == wl.ids).all()
+    np.testing.assert_allclose(to_host(L.w), wl.w, rtol=2e-6, atol=1e-7)
+
+
+@pytest.mark.parametrize("T,E,K", [(1, 8, 2), (37, 512, 10), (5, 256, 8), (64, 1024, 32), (3, 33, 33)])
+def test_route_shapes_and_ties(T, E, K):
+    cfg = SMALL["tiny"].replace(T=T, E=E, K=K, M_max=T)
+    logits = mi.normal(1, 77, (T, E), dtype="f32")
+    logits[0, :] = 0.5                      # a token whose logits all tie
+    if T > 2:
+        logits[2, ::3] = logits[2, 1]       # many exact ties in another
+    ids, w = oracle.route(logits, K)
+    p = moe.Problem.make(T=T, H=64, I=128, E=E, K=K, M_max=T, act="f32", wt="f32", out="f32")
+    gids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    gw = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    moe.moe_route_topk(p, to_dev(logits), gids, gw)
+    torch.cuda.synchronize()
+    assert (to_host(gids) == ids).all()
+    np.testing.assert_allclose(to_host(gw), w, rtol=2e-6, atol=1e-7)
+
+
+# ---- a2 permute -----------------------------------------------------------------
+
+def run_permute(wl, ids=None):
+    L = wl.layer()
+    ids = wl.ids if ids is None else ids
+    L.ids.copy_(torch.from_numpy(np.ascontiguousarray(ids, np.int32)))
+    for t in (L.masked_m, L.offsets, L.row_of, L.src_of):
+        t.fill_(SENT_I32)
+    if L.xg.dtype == torch.uint8:
+        L.xg.fill_(0x5A)
+        L.xg_s.fill_(-3.0)
+    else:
+        L.xg.fill_(-3.0)
+    L.err.zero_()
+    L.permute(to_dev(wl.x))
+    torch.cuda.synchronize()
+    return L
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_permute(workloads, name):
+    wl = workloads[name]
+    cfg = wl.cfg
+    L = run_permute(wl)
+    lay = oracle_layout(wl)
+    assert int(to_host(L.err)[0]) == 0
+    assert (to_host(L.masked_m) == lay["masked_m"]).all()
+    assert (to_host(L.offsets) == lay["offsets"]).all()
+    assert (to_host(L.row_of) == lay["row_of"]).all()
+    valid = lay["src_of"] >= 0
+    src = to_host(L.src_of)
+    assert (src[valid] == lay["src_of"][valid]).all()
+    assert (src[~valid] == SENT_I32).all()  # padding rows untouched
+    xg, xgs = oracle.dispatch_values(cfg, wl.x, lay["row_of"])
+    gx = to_host(L.xg)
+    assert (gx[valid] == xg[valid]).all()  # copies and e4m3 codes bit-exact
+    if cfg.gemm == "e4m3":
+        assert (to_host(L.xg_s)[valid] == xgs[valid]).all()
+        assert (gx[~valid] == 0x5A).all()
+    else:
+        assert (real(gx[~valid], cfg.gemm) == -3.0).all()
+
+
+def test_permute_empty_and_one_hot():
+    cfg = SMALL["e4m3_masked_shared"]
+    wl = Workload(cfg)
+    # every token on experts 0..K-1: the other slots stay empty
+    ids = np.tile(np.arange(cfg.K, dtype=np.int32), (cfg.T, 1))
+    L = run_permute(wl, ids)
+    mm = to_host(L.masked_m)
+    assert (mm[:cfg.K] == cfg.T).all() and (mm[cfg.K:cfg.P] == 0).all() and mm[cfg.P] == cfg.T
+    lay = oracle.layout(cfg, ids, None)
+    assert (to_host(L.row_of) == lay["row_of"]).all()
+
+
+def test_permute_overflow_sets_flag_without_stray_writes():
+    cfg = SMALL["bf16_masked"].replace(M_max=5)
+    wl = Workload(cfg)
+    L = run_permute(wl)
+    lay = oracle.layout(cfg, wl.ids, None)
+    assert lay["status"] == -2
+    assert int(to_host(L.err)[0]) & moe.MOE_FLAG_OVERFLOW
+    assert (to_host(L.masked_m) == lay["masked_m"]).all()  # true counts are reported
+    ro = to_host(L.row_of)
+    ranks_ok = lay["row_of"] % cfg.M_max < cfg.M_max
+    # records past M_max are not placed
+    for t in range(cfg.T):
+        for k in range(cfg.K):
+            s = wl.ids[t, k]
+            rank = (lay["row_of"][t, k] - s * cfg.M_max)
+            assert ro[t, k] == (lay["row_of"][t, k] if rank < cfg.M_max else -1)
+    assert ranks_ok.all()
+
+
+def test_permute_bad_ids_flagged():
+    cfg = SMALL["bf16_masked"]
+    wl = Workload(cfg)
+    ids = wl.ids.copy()
+    ids[3, 0] = cfg.E + 4
+    L = run_permute(wl, ids)
+    assert int(to_host(L.err)[0]) & moe.MOE_FLAG_BAD_EXPERT
+    assert to_host(L.row_of)[3, 0] == -1
+
+
+# ---- a3 / a4 grouped GEMMs -------------------------------------------------------------
+
+def gemm_inputs(wl):
+    cfg = wl.cfg
+    lay = oracle_layout(wl)
+    xg, xgs = oracle.dispatch_values(cfg, wl.x, lay["row_of"])
+    o = wl.order
+    w13, w2 = wl.w13[o], wl.w2[o]
+    w13s = None if wl.w13_s is None else wl.w13_s[o]
+    w2s = None if wl.w2_s is None else wl.w2_s[o]
+    return lay, xg, xgs, w13, w13s, w2, w2s
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_grouped_swiglu(workloads, name):
+    wl = workloads[name]
+    cfg = wl.cfg
+    lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
+    hg_ref, hgs_ref = oracle.grouped_swiglu(cfg, xg, xgs, w13, w13s, lay["masked_m"], lay["offsets"])
+    L = wl.layer()
+    L.xg.copy_(to_dev(xg))
+    if xgs is not None:
+        L.xg_s.copy_(to_dev(xgs))
+    L.masked_m.copy_(to_dev(lay["masked_m"]))
+    L.offsets.copy_(to_dev(lay["offsets"]))
+    if L.hg.dtype == torch.uint8:
+        L.hg.fill_(0x5A)
+    else:
+        L.hg.fill_(-3.0)
+    L.swiglu()
+    torch.cuda.synchronize()
+    assert int(to_host(L.err)[0]) == 0
+    valid = lay["src_of"] >= 0
+    got = real(to_host(L.hg)[valid], cfg.gemm, None if hgs_ref is None else to_host(L.hg_s)[valid])
+    ref = real(hg_ref[valid], cfg.gemm, None if hgs_ref is None else hgs_ref[valid])
+    assert rel_err(got, ref) <= TOL[cfg.gemm]
+    pad = to_host(L.hg)[~valid]
+    assert (pad == 0x5A).all() if cfg.gemm == "e4m3" else (real(pad, cfg.gemm) == -3.0).all()
+
+
+@pytest.mark.parametrize("name", NAMES)
+def test_grouped_down(workloads, name):
+    wl = workloads[name]
+    cfg = wl.cfg
+    lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
+    hg, hgs = oracle.grouped_swiglu(cfg, xg, xgs, w13, w13s, lay["masked_m"], lay["offsets"])
+    yg_ref = oracle.grouped_down(cfg, hg, hgs, w2, w2s, lay["masked_m"], lay["offsets"])
+    L = wl.layer()
+    L.hg.copy_(to_dev(hg))
+    if hgs is not None:
+        L.hg_s.copy_(to_dev(hgs))
+    L.masked_m.copy_(to_dev(lay["masked_m"]))
+    L.offsets.copy_(to_dev(lay["offsets"]))
+    L.yg.fill_(-3.0)
+    L.down()
+    torch.cuda.synchronize()
+    assert int(to_host(L.err)[0]) == 0
+    valid = lay["src_of"] >= 0
+    got = real(to_host(L.yg)[valid], cfg.y_dtype)
+    ref = real(yg_ref[valid], cfg.y_dtype)
+    assert rel_err(got, ref) <= TOL[cfg.gemm]
+    assert (real(to_host(L.yg)[~valid], cfg.y_dtype) == -3.0).all()
+
+
+# ---- a5 combine ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", NAMES)
+def test_combine(workloads, name):
+    wl = workloads[name]
+    cfg = wl.cfg
+    lay = oracle_layout(wl)
+    rows = cfg.rows
+    yg = mi.normal(9, 55, (rows, cfg.H), dtype="f32" if cfg.y_dtype == "f32" else "bf16")
+    w32 = wl.w.astype(np.float32)
+    out_ref, exact = oracle.combine(cfg, yg, lay["row_of"], w32)
+    L = wl.layer()
+    L.yg.copy_(to_dev(yg))
+    L.row_of.copy_(to_dev(lay["row_of"]))
+    L.w.copy_(to_dev(w32))
+    L.combine()
+    torch.cuda.synchronize()
+    got = real(to_host(L.out), cfg.out)
+    # fp32 sum of the same stored values, one rounding: at most one output ulp apart
+    ulp = 2.0 ** -7 if cfg.out == "bf16" else 2.0 ** -20
+    assert (np.abs(got - exact) <= ulp * np.abs(exact) + 1e-30).all()
+    assert rel_err(got, real(out_ref, cfg.out)) <= TOL[cfg.out]
+
+
+# ---- two-level accumulation ("Inference INFRA methodology (5)", section "DeepGEMM") ----
+
+def test_fp8_promotion_deep_k_all_positive():
+    """All-positive data and K = 16384: with the 128-K promotion to fp32 the down
+    GEMM stays at bf16-output accuracy; the page reports about 0.17% with the
+    two-level scheme against about 25% without it on its hardware."""
+    cfg = SMALL["e4m3_masked_shared"].replace(name="deepk", T=8, H=256, I=16384, E=1, K=1, shared=0, M_max=8)
+    rng = np.random.default_rng(0)
+    hq = oracle.e4m3_encode(rng.uniform(0.5, 448.0, (cfg.T * 1, cfg.I)).astype(np.float32))
+    hs = np.full((cfg.T, cfg.I // 128), 1.0 / 448.0, np.float32)
+    wq = oracle.e4m3_encode(rng.uniform(0.5, 448.0, (1, cfg.H, cfg.I)).astype(np.float32))
+    ws = np.full((1, cfg.H // 128, cfg.I // 128), 1.0 / 448.0, np.float32)
+    masked_m = np.array([cfg.T], np.int32)
+    offsets = np.array([0, cfg.T], np.int32)
+    ref = oracle.grouped_down(cfg, hq, hs, wq, ws, masked_m, offsets)
+    exact = oracle.dequant(hq, "e4m3", hs, 1) @ oracle.dequant(wq[0], "e4m3", ws[0], 128).T
+    p = moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=1, K=1, M_max=cfg.T, act="bf16", wt="e4m3", out="bf16")
+    yg = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    ws_t = torch.empty(max(moe.moe_workspace_bytes(p), 256), dtype=torch.uint8, device="cuda")
+    moe.moe_grouped_down_gemm(p, to_dev(hq), to_dev(hs), to_dev(wq), to_dev(ws), to_dev(masked_m),
+                              to_dev(offsets), yg, err, ws_t)
+    torch.cuda.synchronize()
+    got = real(to_host(yg), "bf16")
+    rel = np.abs(got - exact) / np.abs(exact)
+    assert rel.max() < 0.004  # bf16 output rounding is 2^-9 = 0.2%
+    assert rel_err(got, real(ref, "bf16")) < 0.004
+
+
+# ---- determinism ---------------------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["bf16_masked", "e4m3_eplb_zipf", "e4m3_contig"])
+def test_rerun_bitwise_identical(workloads, name):
+    wl = workloads[name]
+    L = wl.layer()
+    x, lg = to_dev(wl.x), to_dev(wl.logits)
+    a = to_host(L.forward(x, lg).clone())
+    for _ in range(2):
+        b = to_host(L.forward(x, lg).clone())
+        assert (a == b).all()
