@@ -160,6 +160,31 @@ moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, 
                        float* xg_scales, int32_t* err_flag, void* workspace, size_t workspace_bytes,
                        moe_stream_t stream);
 
+/* moe_permute for callers that cannot allocate device memory.  The pages
+ * describe no such variant; it is an addition of this library.
+ * Some callers cannot call cudaMalloc where they run the layer: an inference
+ * engine plugin whose enqueue step must not allocate, code running while its
+ * stream is being captured into a CUDA graph, a framework whose device memory
+ * all belongs to its own pool.  This call takes the same arguments and writes
+ * the same outputs as moe_permute, but needs no workspace: its scratch is a
+ * fixed 4 MiB array inside the library, which every GPU that loads the library
+ * keeps until the process exits.
+ *   - A problem whose scratch exceeds 4 MiB is rejected with MOE_ERR_WORKSPACE
+ *     before anything is enqueued (the scratch is 8*P*ceil(T/32) + 4*T*K +
+ *     4*E*(P-E+2) bytes, each term rounded up to 256; the prefill workload
+ *     T=8192, E=P=512, K=10 needs about 1.3 MiB).
+ *   - The first call on a device looks up the array's device address (with
+ *     that device current) and keeps it; make that first call outside of any
+ *     stream capture.
+ *   - All calls share the one array, which keeps the previous call's contents
+ *     (the call clears what must start at zero itself).  Calls that overlap on
+ *     the GPU -- on different streams, or from different threads, without
+ *     ordering between them -- race on it and give wrong results. */
+moe_status moe_permute_no_workspace(const moe_problem* p, const int32_t* ids, const void* x,
+                                    const int32_t* phys_to_log, int32_t* masked_m, int32_t* offsets,
+                                    int32_t* row_of, int32_t* src_of, void* xg, float* xg_scales, int32_t* err_flag,
+                                    moe_stream_t stream);
+
 /* Step 3 (expert gate/up; "MoE inference and expert parallelism", routing
  * section: SwiGLU with W1 = gate, W3 = up; "Inference INFRA methodology (5)",
  * section "DeepGEMM": masked_m read on the device, no MMA for padding tiles,

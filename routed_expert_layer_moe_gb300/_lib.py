@@ -23,7 +23,7 @@ LAYOUTS = {"masked": MOE_LAYOUT_MASKED, "contig": MOE_LAYOUT_CONTIG}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_version", "moe_status_string", "moe_grouped_rows", "moe_workspace_bytes", "moe_check_problem",
-           "moe_route_topk", "moe_permute", "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_combine",
+           "moe_route_topk", "moe_permute", "moe_permute_no_workspace", "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_combine",
            "moe_eplb_invert"]
 
 
@@ -74,6 +74,8 @@ def lib():
     L.moe_route_topk.restype = i32
     L.moe_permute.argtypes = [pp] + [vp] * 11 + [sz, vp]
     L.moe_permute.restype = i32
+    L.moe_permute_no_workspace.argtypes = [pp] + [vp] * 11
+    L.moe_permute_no_workspace.restype = i32
     L.moe_grouped_swiglu_gemm.argtypes = [pp] + [vp] * 10 + [sz, vp]
     L.moe_grouped_swiglu_gemm.restype = i32
     L.moe_grouped_down_gemm.argtypes = [pp] + [vp] * 9 + [sz, vp]
@@ -138,6 +140,15 @@ def moe_permute(p: Problem, ids, x, phys_to_log, masked_m, offsets, row_of, src_
     _check(lib().moe_permute(ctypes.byref(p), _ptr(ids), _ptr(x), _ptr(phys_to_log), _ptr(masked_m),
                              _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(xg), _ptr(xg_scales),
                              _ptr(err_flag), _ptr(workspace), nbytes, _stream(stream)), "moe_permute")
+
+
+def moe_permute_no_workspace(p: Problem, ids, x, phys_to_log, masked_m, offsets, row_of, src_of, xg, xg_scales,
+                             err_flag, stream=None) -> None:
+    """moe_permute without a workspace argument, for callers that cannot allocate
+    device memory; its scratch is a fixed array inside the library (see moe.h)."""
+    _check(lib().moe_permute_no_workspace(ctypes.byref(p), _ptr(ids), _ptr(x), _ptr(phys_to_log), _ptr(masked_m),
+                                          _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(xg), _ptr(xg_scales),
+                                          _ptr(err_flag), _stream(stream)), "moe_permute_no_workspace")
 
 
 def moe_grouped_swiglu_gemm(p: Problem, xg, xg_scales, w13, w13_scales, masked_m, offsets, hg, hg_scales,
