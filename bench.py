@@ -389,9 +389,17 @@ def main():
     ap.add_argument("--config", default=HEADLINE, choices=list(mi.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--override", default="",
+                    help="comma-separated field=value changes to the workload, e.g. T=2048,E=128 (profiling cases)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     cfg = mi.CONFIGS[args.config]
+    if args.override:
+        kw = {}
+        for item in args.override.split(","):
+            k, v = item.split("=")
+            kw[k.strip()] = type(getattr(cfg, k.strip()))(v)
+        cfg = cfg.replace(name=cfg.name + "[" + args.override + "]", **kw)
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
