@@ -186,7 +186,7 @@ static moe_status gemm_call(const moe_problem* p, int mode, const void* act, con
   if (!act || !w || !masked_m || !offsets || !out || !err_flag) return MOE_ERR_INVALID;
   if (p->wt == MOE_E4M3 && (!act_scales || !w_scales)) return MOE_ERR_INVALID;
   if (p->wt == MOE_E4M3 && mode == MODE_SWIGLU && !out_scales) return MOE_ERR_INVALID;
-  if (!aligned16(act) || !aligned16(w)) return MOE_ERR_UNSUPPORTED;
+  if (!aligned16(act) || !aligned16(w) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
   if (workspace_bytes < ws_bytes(*p) || (ws_bytes(*p) > 0 && !workspace)) return MOE_ERR_WORKSPACE;
   return launched(launch_gemm(*p, mode, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err_flag,
                               workspace, (cudaStream_t)stream));

@@ -11,49 +11,63 @@
 // the expert is SwiGLU with W1 = gate, W3 = up, W2 = down.
 //
 // Design (GB300, one CTA per SM, persistent):
-//   * Swap-AB: the weights fill the MMA's M = 128 side and the tokens of one
-//     expert (up to 128 per unit) its N side, so a decode expert with a
-//     handful of tokens still streams its weights once at full width, and N
-//     is rounded only to 16 (no MMA for padding past that).
-//   * A unit is (slot s, token chunk c of 128 rows, tile pair j, K split q).
-//     Gate/up: the pair is the gate tile rows [128j, 128j+128) and the up tile
-//     at rows I + 128j, sharing one B (token) tile.  Down: two consecutive
-//     128-row tiles of W2.  Units exist only for chunks with at least one real
-//     row: the kernel builds the unit list from masked_m on the device.
-//   * Warp 0: TMA producer (weights with an evict-first L2 hint; token tile
-//     with a box of 16/32/64/128 rows, the smallest that covers the chunk).
-//     Warp 1: tensor-memory allocator and the single MMA-issuing thread.
-//     Warps 2-9: epilogue, two warps per tensor-memory lane quarter, each
-//     owning 64 of the 128 token columns.
-//   * FP8: the MMA writes each 128-K block into one of two tensor-memory
-//     buffers; the epilogue reads it, scales by s_w * s_x and adds into
-//     registers while the MMA fills the other buffer.  BF16: the whole K range
-//     accumulates in tensor memory; the two buffers alternate between units.
+//   * A unit is (slot s, token chunk c, tile pair j, K split q).  A slot's rows
+//     are split into ceil(rows/128) chunks of near-equal size, so the chunks of
+//     one expert take the same time and re-read its weights from L2 together.
+//     Gate/up: the pair is the gate tile (rows [128j, 128j+128) of W1) and the
+//     up tile (same rows of W3).  Down: two consecutive 128-row tiles of W2.
+//     Units exist only for chunks with rows: each CTA builds the unit list from
+//     masked_m on the device at kernel start.
+//   * Two orientations, chosen per launch from the problem's expected rows per
+//     expert:
+//       - weight-major (decode): the weight tile is the MMA's M = 128 side and
+//         the chunk's tokens its N side, rounded up to 16 -- a decode expert
+//         with a few tokens streams its weights at full width and issues N = 16
+//         MMAs;
+//       - token-major (prefill): the 128 token rows are the M side and the gate
+//         and up tiles together one N = 256 MMA; the activation scale becomes
+//         one value per thread and the SwiGLU and the stores are row-local.
+//   * Warp 0: TMA producer (weights with an evict-first L2 hint).  Warp 1:
+//     tensor-memory allocator and the single MMA-issuing thread.  Warps 2-3:
+//     FP8 scale loaders (a unit's activation and weight scales into a double
+//     buffer in shared memory).  Warps 4-11: epilogue, two warps per
+//     tensor-memory lane quarter.
+//   * FP8: the MMAs of one 128-K block write one of two tensor-memory buffers;
+//     the epilogue reads it, scales it and adds it into fp32 registers while
+//     the MMA fills the other.  BF16: the whole K range accumulates in tensor
+//     memory; the two buffers alternate between units.
 //   * Every wait is bounded in time; on expiry the CTA sets an abort flag,
 //     drains its copies and MMAs, frees tensor memory, reports
 //     MOE_FLAG_TIMEOUT and returns.
 #include <algorithm>
+#include <cmath>
 
 #include "common.cuh"
 
 namespace moe {
 namespace {
 
-constexpr int BM = 128;                      // weight rows per tile (MMA M)
-constexpr int BN = 128;                      // tokens per unit (largest MMA N used)
-constexpr int ROW_BYTES = 128;               // K bytes per stage row (one 128-byte swizzle span)
+constexpr int BM = 128;             // rows of one weight tile
+constexpr int BN = 128;             // token rows of one chunk at most
+constexpr int ROW_BYTES = 128;      // K bytes per stage row (one 128-byte swizzle span)
 constexpr int TILE_A_BYTES = BM * ROW_BYTES;
 constexpr int TILE_B_BYTES = BN * ROW_BYTES;
-constexpr int STAGE_BYTES = 2 * TILE_A_BYTES + TILE_B_BYTES;
-constexpr int NUM_THREADS = 384;  // three warpgroups
-constexpr int EPI_THREADS = 256;  // warpgroups 1 and 2
+constexpr int STAGE_BYTES = 2 * TILE_A_BYTES + TILE_B_BYTES;  // weight tile 0 | weight tile 1 | token tile
+constexpr int NUM_THREADS = 384;    // three warpgroups
+constexpr int EPI_THREADS = 256;    // warpgroups 1 and 2
 constexpr int EPI_WARP0 = 4;
-// Register split (setmaxnreg): warpgroup 0 (TMA + MMA) gives registers to the
-// two epilogue warpgroups, which hold 2 x 64 fp32 accumulators per thread.
-// 4*32*REGS_CTRL + 8*32*REGS_EPI must not exceed 384 * (registers at launch).
-constexpr int REGS_CTRL = 64;
-constexpr int REGS_EPI = 216;
-constexpr int REGS_NEEDED = 4 * 32 * REGS_CTRL + 8 * 32 * REGS_EPI;
+constexpr int LOAD_WARP0 = 2;       // warps 2 and 3 load FP8 scales
+constexpr int LOAD_THREADS = 64;
+// Register split (setmaxnreg): warpgroup 0 (TMA, MMA, scale loads) gives
+// registers to the two epilogue warpgroups, which hold 2 x 64 fp32
+// accumulators per thread.  4*32*ctrl + 8*32*epi must not exceed
+// 384 * (registers at launch); the launcher checks it before the first launch.
+template <bool F8>
+struct Regs {
+  static constexpr int ctrl = F8 ? 72 : 80;
+  static constexpr int epi = F8 ? 216 : 208;
+  static constexpr int needed = 4 * 32 * ctrl + 8 * 32 * epi;
+};
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t TIMEOUT_NS = 2000000000ull;
 
@@ -83,10 +97,11 @@ struct TcParams {
 
 struct Unit {
   int s, c, j, q;
-  int nvalid;
-  int rowB, rowA0, rowA1;
+  int nvalid;           // token rows of the chunk
+  int rowB;             // first grouped-buffer row of the chunk
+  int rowA0, rowA1;     // first weight row of tile 0 / tile 1
   int kb0, kb1;
-  bool a1;
+  bool a1;              // tile 1 exists
 };
 
 __device__ __forceinline__ int slot_rows(const TcParams& p, int s) {
@@ -114,8 +129,9 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* prefix
   const int rest = r / p.ksplit;
   U.c = rest % nch;
   U.j = rest / nch;
-  U.nvalid = min(BN, m - U.c * BN);
-  U.rowB = (p.masked ? lo * p.M_max : __ldg(p.offsets + lo)) + U.c * BN;
+  const int base = m / nch, extra = m - base * nch;  // near-equal chunks
+  U.nvalid = base + (U.c < extra ? 1 : 0);
+  U.rowB = (p.masked ? lo * p.M_max : __ldg(p.offsets + lo)) + U.c * base + min(U.c, extra);
   U.rowA0 = lo * p.NA + U.j * p.pair_stride;
   U.rowA1 = U.rowA0 + p.a1_off;
   U.a1 = (MODE == MODE_SWIGLU) ? true : (U.j * p.pair_stride + p.a1_off < p.NA);
@@ -124,27 +140,36 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* prefix
   return U;
 }
 
-template <typename T>
-__device__ __forceinline__ void store_bf16(T* base, size_t idx, float v) {
-  reinterpret_cast<__nv_bfloat16*>(base)[idx] = __float2bfloat16_rn(v);
+__device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
+  const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+  return *reinterpret_cast<const uint32_t*>(&v);
 }
 
-template <bool F8, int MODE>
+__device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
+  const __nv_fp8x2_storage_t lo = __nv_cvt_float2_to_fp8x2(make_float2(a, b), __NV_SATFINITE, __NV_E4M3);
+  const __nv_fp8x2_storage_t hi = __nv_cvt_float2_to_fp8x2(make_float2(c, d), __NV_SATFINITE, __NV_E4M3);
+  return (uint32_t)lo | ((uint32_t)hi << 16);
+}
+
+template <bool F8, int MODE, bool TM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
                            const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
                            const __grid_constant__ CUtensorMap tmB128, const TcParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [kb_per_split][BN] activation scales
-  float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [2][kb_per_split] weight scales
-  float* red = reinterpret_cast<float*>(smem + p.red_off);  // [2 halves][4 quarters][64] column maxima
+  const int KBS = p.kb_per_split;
+  float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [2 bufs][KBS][BN] activation scales, [k][row]
+  float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [2 bufs][2 tiles][KBS] weight scales
+  float* red = reinterpret_cast<float*>(smem + p.red_off);  // [2 parities][512] group maxima
   int* prefix = reinterpret_cast<int*>(smem + p.pre_off);   // [nslots + 1] unit prefix
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
-  uint64_t* tfull = empty + p.stages;  // [2]
-  uint64_t* tempty = tfull + 2;        // [2]
-  uint64_t* drain = tempty + 2;        // [1]
+  uint64_t* tfull = empty + p.stages;  // [2] accumulator buffer written
+  uint64_t* tempty = tfull + 2;        // [2] accumulator buffer read
+  uint64_t* sfull = tempty + 2;        // [2] scale buffer loaded
+  uint64_t* sempty = sfull + 2;        // [2] scale buffer consumed
+  uint64_t* drain = sempty + 2;        // [1]
   uint64_t* ebar = drain + 1;          // [1] all epilogue threads
   uint64_t* hbar = ebar + 1;           // [2] the 128 epilogue threads of one column half
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + p.misc_off);
@@ -162,11 +187,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
       mbar_init(&tempty[i], EPI_THREADS);
+      mbar_init(&sfull[i], LOAD_THREADS);
+      mbar_init(&sempty[i], EPI_THREADS);
+      mbar_init(&hbar[i], 128);
     }
     mbar_init(drain, 1);
     mbar_init(ebar, EPI_THREADS);
-    mbar_init(&hbar[0], 128);
-    mbar_init(&hbar[1], 128);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -200,154 +226,207 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_base_smem;
   const int total = prefix[p.nslots];
+
   if (warp < EPI_WARP0) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_CTRL));
-  if (warp == 0) {
-    // ------------------------------------------------------------ producer
-    if (lane == 0) {
-      tma_prefetch_map(&tmA);
-      tma_prefetch_map(&tmB16);
-      tma_prefetch_map(&tmB32);
-      tma_prefetch_map(&tmB64);
-      tma_prefetch_map(&tmB128);
-      const uint64_t pol = policy_evict_first();
-      const int kb_elems = F8 ? ROW_BYTES : ROW_BYTES / 2;
-      int stage = 0;
-      uint32_t phase = 0;
-      long issued = 0;
-      bool ok = true;
-      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
-        const Unit U = decode_unit<MODE>(p, prefix, u);
-        const CUtensorMap* mb;
-        int box;
-        if (U.nvalid <= 16) {
-          mb = &tmB16;
-          box = 16;
-        } else if (U.nvalid <= 32) {
-          mb = &tmB32;
-          box = 32;
-        } else if (U.nvalid <= 64) {
-          mb = &tmB64;
-          box = 64;
-        } else {
-          mb = &tmB128;
-          box = 128;
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<F8>::ctrl));
+    if (warp == 0) {
+      // ------------------------------------------------------------ producer
+      if (lane == 0) {
+        tma_prefetch_map(&tmA);
+        tma_prefetch_map(&tmB128);
+        if (!TM) {
+          tma_prefetch_map(&tmB16);
+          tma_prefetch_map(&tmB32);
+          tma_prefetch_map(&tmB64);
         }
-        const uint32_t bytes = TILE_A_BYTES * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT_NS)) {
-            ok = false;
-            break;
+        const uint64_t pol = policy_evict_first();
+        const int kb_elems = F8 ? ROW_BYTES : ROW_BYTES / 2;
+        int stage = 0;
+        uint32_t phase = 0;
+        long issued = 0;
+        bool ok = true;
+        for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+          const Unit U = decode_unit<MODE>(p, prefix, u);
+          const CUtensorMap* mb = &tmB128;
+          int box = 128;
+          if (!TM) {
+            if (U.nvalid <= 16) {
+              mb = &tmB16;
+              box = 16;
+            } else if (U.nvalid <= 32) {
+              mb = &tmB32;
+              box = 32;
+            } else if (U.nvalid <= 64) {
+              mb = &tmB64;
+              box = 64;
+            }
           }
-          uint8_t* sA0 = smem + (size_t)stage * STAGE_BYTES;
-          mbar_arrive_expect_tx(&full[stage], bytes);
-          const int x = kb * kb_elems;
-          tma_load_2d_hint(sA0, &tmA, &full[stage], x, U.rowA0, pol);
-          if (U.a1) tma_load_2d_hint(sA0 + TILE_A_BYTES, &tmA, &full[stage], x, U.rowA1, pol);
-          tma_load_2d(sA0 + 2 * TILE_A_BYTES, mb, &full[stage], x, U.rowB);
-          ++issued;
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
+          const uint32_t bytes = TILE_A_BYTES * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
+          for (int kb = U.kb0; kb < U.kb1; ++kb) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT_NS)) {
+              ok = false;
+              break;
+            }
+            uint8_t* st = smem + (size_t)stage * STAGE_BYTES;
+            mbar_arrive_expect_tx(&full[stage], bytes);
+            const int x = kb * kb_elems;
+            tma_load_2d_hint(st, &tmA, &full[stage], x, U.rowA0, pol);
+            if (U.a1) tma_load_2d_hint(st + TILE_A_BYTES, &tmA, &full[stage], x, U.rowA1, pol);
+            tma_load_2d(st + 2 * TILE_A_BYTES, mb, &full[stage], x, U.rowB);
+            ++issued;
+            if (++stage == p.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) {
+          // let the copies already in flight land before the CTA's shared memory is released
+          const long first = issued > p.stages ? issued - p.stages : 0;
+          for (long i = first; i < issued; ++i) {
+            const int st = (int)(i % p.stages);
+            const uint32_t ph = (uint32_t)((i / p.stages) & 1);
+            const uint64_t t0 = global_timer_ns();
+            while (!mbar_try_wait(&full[st], ph) && global_timer_ns() - t0 < TIMEOUT_NS) {
+            }
           }
         }
       }
-      if (!ok) {
-        // let the copies already in flight land before the CTA's shared memory is released
-        const long first = issued > p.stages ? issued - p.stages : 0;
-        for (long i = first; i < issued; ++i) {
-          const int st = (int)(i % p.stages);
-          const uint32_t ph = (uint32_t)((i / p.stages) & 1);
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(&full[st], ph) && global_timer_ns() - t0 < TIMEOUT_NS) {
-          }
-        }
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
-      uint32_t acc_it = 0;
-      bool ok = true;
-      bool any = false;
-      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
-        const Unit U = decode_unit<MODE>(p, prefix, u);
-        const int N = (U.nvalid + 15) & ~15;
-        const uint32_t idesc = mma_idesc<F8>(BM, N);
-        uint32_t b = 0;
-        if constexpr (!F8) {
-          b = acc_it & 1u;
-          if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-        }
-        for (int kb = U.kb0; kb < U.kb1; ++kb) {
-          if constexpr (F8) {
+    } else if (warp == 1) {
+      // ------------------------------------------------------------ MMA issuer
+      if (lane == 0) {
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t acc_it = 0;
+        bool ok = true;
+        bool any = false;
+        for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+          const Unit U = decode_unit<MODE>(p, prefix, u);
+          // weight-major: M = 128 weight rows, N = tokens rounded to 16 (one MMA per tile);
+          // token-major: M = 128 token rows, N = both weight tiles (one MMA)
+          const uint32_t idesc = TM ? mma_idesc<F8>(BM, U.a1 ? 2 * BM : BM)
+                                    : mma_idesc<F8>(BM, (U.nvalid + 15) & ~15);
+          uint32_t b = 0;
+          if constexpr (!F8) {
             b = acc_it & 1u;
             if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
               ok = false;
               break;
             }
+            tc_fence_after_sync();
           }
-          if (!mbar_wait(&full[stage], phase, abort_flag, TIMEOUT_NS)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after_sync();
-          const uint32_t a0 = smem_u32(smem + (size_t)stage * STAGE_BYTES);
-          const uint64_t da0 = smem_desc_sw128(a0);
-          const uint64_t da1 = smem_desc_sw128(a0 + TILE_A_BYTES);
-          const uint64_t db = smem_desc_sw128(a0 + 2 * TILE_A_BYTES);
-          const uint32_t d0 = tmem_base + b * 256u;
-          const uint32_t d1 = d0 + 128u;
+          for (int kb = U.kb0; kb < U.kb1; ++kb) {
+            if constexpr (F8) {
+              b = acc_it & 1u;
+              if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
+                ok = false;
+                break;
+              }
+            }
+            if (!mbar_wait(&full[stage], phase, abort_flag, TIMEOUT_NS)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after_sync();
+            const uint32_t st = smem_u32(smem + (size_t)stage * STAGE_BYTES);
+            const uint64_t dw0 = smem_desc_sw128(st);
+            const uint64_t dw1 = smem_desc_sw128(st + TILE_A_BYTES);
+            const uint64_t dtok = smem_desc_sw128(st + 2 * TILE_A_BYTES);
+            const uint32_t d0 = tmem_base + b * 256u;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
-            const uint32_t acc = F8 ? (ks > 0) : (kb > U.kb0 || ks > 0);
-            tc_mma<F8>(d0, da0 + 2 * ks, db + 2 * ks, idesc, acc);
-            if (U.a1) tc_mma<F8>(d1, da1 + 2 * ks, db + 2 * ks, idesc, acc);
+            for (int ks = 0; ks < 4; ++ks) {
+              const uint32_t acc = F8 ? (ks > 0) : (kb > U.kb0 || ks > 0);
+              if constexpr (TM) {
+                tc_mma<F8>(d0, dtok + 2 * ks, dw0 + 2 * ks, idesc, acc);
+              } else {
+                tc_mma<F8>(d0, dw0 + 2 * ks, dtok + 2 * ks, idesc, acc);
+                if (U.a1) tc_mma<F8>(d0 + 128u, dw1 + 2 * ks, dtok + 2 * ks, idesc, acc);
+              }
+            }
+            any = true;
+            tc_commit(&empty[stage]);
+            if constexpr (F8) {
+              tc_commit(&tfull[b]);
+              ++acc_it;
+            }
+            if (++stage == p.stages) {
+              stage = 0;
+              phase ^= 1u;
+            }
           }
-          any = true;
-          tc_commit(&empty[stage]);
-          if constexpr (F8) {
-            tc_commit(&tfull[b]);
-            ++acc_it;
-          }
-          if (++stage == p.stages) {
-            stage = 0;
-            phase ^= 1u;
+          if constexpr (!F8) {
+            if (ok) {
+              tc_commit(&tfull[b]);
+              ++acc_it;
+            }
           }
         }
-        if constexpr (!F8) {
-          if (ok) {
-            tc_commit(&tfull[b]);
-            ++acc_it;
+        if (!ok && any) {
+          // all MMAs issued by this thread must finish before tensor memory is freed
+          tc_commit(drain);
+          const uint64_t t0 = global_timer_ns();
+          while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < TIMEOUT_NS) {
           }
         }
       }
-      if (!ok && any) {
-        // all MMAs issued by this thread must finish before tensor memory is freed
-        tc_commit(drain);
-        const uint64_t t0 = global_timer_ns();
-        while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < TIMEOUT_NS) {
+    } else if (F8) {
+      // ------------------------------------------------------------ FP8 scale loaders
+      const int lt = tid - LOAD_WARP0 * 32;
+      uint32_t it = 0;
+      for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+        const Unit U = decode_unit<MODE>(p, prefix, u);
+        const uint32_t sb = it & 1u;
+        if (!mbar_wait(&sempty[sb], ((it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) break;
+        const int n = U.nvalid, nkb = U.kb1 - U.kb0;
+        float* sxb = sx + (size_t)sb * KBS * BN;
+        // one thread per token row: its nkb scales are contiguous in global memory; read them
+        // with independent 16-byte loads, store them transposed ([k][row], conflict-free)
+        for (int c = lt; c < n; c += LOAD_THREADS) {
+          const float* src = p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + U.kb0;
+          if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+            constexpr int VB = 4;
+            for (int k0 = 0; k0 < nkb; k0 += 4 * VB) {
+              float4 v[VB];
+#pragma unroll
+              for (int b = 0; b < VB; ++b)
+                if (k0 + 4 * b + 3 < nkb) v[b] = __ldg(reinterpret_cast<const float4*>(src + k0 + 4 * b));
+#pragma unroll
+              for (int b = 0; b < VB; ++b) {
+                const int k = k0 + 4 * b;
+                if (k + 3 < nkb) {
+                  sxb[(k + 0) * BN + c] = v[b].x;
+                  sxb[(k + 1) * BN + c] = v[b].y;
+                  sxb[(k + 2) * BN + c] = v[b].z;
+                  sxb[(k + 3) * BN + c] = v[b].w;
+                } else {
+                  for (int kk = k; kk < nkb && kk < k + 4; ++kk) sxb[kk * BN + c] = __ldg(src + kk);
+                }
+              }
+            }
+          } else {
+            for (int k = 0; k < nkb; ++k) sxb[k * BN + c] = __ldg(src + k);
+          }
         }
+        float* swb = sw + (size_t)sb * 2 * KBS;
+        const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
+        for (int k = lt; k < nkb; k += LOAD_THREADS) {
+          swb[k] = __ldg(p.a_scales + (size_t)ra0 * p.scale_cols + U.kb0 + k);
+          swb[KBS + k] = U.a1 ? __ldg(p.a_scales + (size_t)ra1 * p.scale_cols + U.kb0 + k) : 0.0f;
+        }
+        mbar_arrive(&sfull[sb]);
       }
     }
-  }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_EPI));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<F8>::epi));
     // ------------------------------------------------------------ epilogue
     const int etid = tid - EPI_WARP0 * 32;
-    const int ew = warp - EPI_WARP0;
-    const int quarter = warp & 3;  // tensor-memory lane quarter this warp may access
-    const int half = ew >> 2;      // token columns [64*half, 64*half + 64) (warpgroup 1 or 2)
-    const int lrow = quarter * 32 + lane;
+    const int quarter = warp & 3;             // tensor-memory lane quarter this warp may access
+    const int half = (warp - EPI_WARP0) >> 2; // column half (warpgroup 1 or 2)
+    const int lrow = quarter * 32 + lane;     // tensor-memory lane of this thread
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    uint32_t acc_it = 0;
-    uint32_t ephase = 0, hphase = 0;
+    uint32_t acc_it = 0, s_it = 0, u_it = 0;
+    uint32_t ephase = 0;
+    uint32_t hphase[2] = {0, 0};
     bool ok = true;
     const size_t oc = (size_t)p.out_cols;
     // bounded barriers among the epilogue threads (a plain bar.sync could not give up)
@@ -359,58 +438,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     auto half_sync = [&](int h) {
       mbar_arrive(&hbar[h]);
-      const bool r = mbar_wait(&hbar[h], hphase, abort_flag, TIMEOUT_NS);
-      hphase ^= 1u;
+      const bool r = mbar_wait(&hbar[h], hphase[h], abort_flag, TIMEOUT_NS);
+      hphase[h] ^= 1u;
       return r;
     };
-    for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+    for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++u_it) {
       const Unit U = decode_unit<MODE>(p, prefix, u);
-      const int c_lo = half * 64;
-      const int ncols = max(0, min(64, U.nvalid - c_lo));
-      const int nch = (ncols + 15) >> 4;
       const int nkb = U.kb1 - U.kb0;
       const bool split = p.ksplit > 1;
-      // output column of this lane for tile 0 / tile 1 of the pair
-      const int col0 = (MODE == MODE_SWIGLU) ? U.j * BM + lrow : U.j * p.pair_stride + lrow;
-      const int col1 = col0 + BM;
-
-      // writes the final values of token column c (0..BN) for this lane
-      auto finish = [&](int c, float v0, float v1) {
-        const size_t row = (size_t)(U.rowB + c);
-        if constexpr (MODE == MODE_SWIGLU) {
-          const float h = silu(v0) * v1;
-          if constexpr (!F8) {
-            store_bf16(p.out, row * oc + col0, h);
-          } else {
-            (void)h;  // e4m3 output is finished group-wise below
-          }
-        } else {
-          store_bf16(p.out, row * oc + col0, v0);
-          if (U.a1) store_bf16(p.out, row * oc + col1, v1);
-        }
-      };
+      // weight-major: this thread owns weight row lrow of each tile and token columns
+      // [c_lo, c_lo + ncols); token-major: token row lrow and weight columns [64*half, +64)
+      const int c_lo = half * 64;
+      const int ncols = TM ? 64 : max(0, min(64, U.nvalid - c_lo));
+      const int npair = (ncols + 31) >> 5;  // 32-column loads
+      float acc0[64], acc1[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        acc0[i] = 0.0f;
+        acc1[i] = 0.0f;
+      }
 
       if constexpr (F8) {
-        float acc0[64], acc1[64];
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          acc0[i] = 0.0f;
-          acc1[i] = 0.0f;
-        }
-        if (!epi_sync()) break;  // readers of the previous unit's scales are done
-        {
-          const int n = U.nvalid;
-          for (int i = etid; i < n * nkb; i += EPI_THREADS) {
-            const int c = i / nkb, k = i - c * nkb;
-            sx[k * BN + c] = __ldg(p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + U.kb0 + k);
-          }
-          const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
-          for (int k = etid; k < nkb; k += EPI_THREADS) {
-            sw[k] = __ldg(p.a_scales + (size_t)ra0 * p.scale_cols + U.kb0 + k);
-            sw[p.kb_per_split + k] = U.a1 ? __ldg(p.a_scales + (size_t)ra1 * p.scale_cols + U.kb0 + k) : 0.0f;
-          }
-        }
-        if (!epi_sync()) break;
+        const uint32_t sb = s_it & 1u;
+        if (!mbar_wait(&sfull[sb], (s_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) break;
+        const float* sxb = sx + (size_t)sb * KBS * BN;
+        const float* swb = sw + (size_t)sb * 2 * KBS;
         for (int k = 0; k < nkb; ++k) {
           const uint32_t b = acc_it & 1u;
           if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
@@ -418,19 +470,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const float s0 = sw[k], s1 = sw[p.kb_per_split + k];
-          const float* sxk = sx + k * BN + c_lo;
+          const float s0 = swb[k], s1 = swb[KBS + k];
+          if constexpr (TM) {
+            const float xs = sxb[k * BN + lrow];
+            const float p0 = s0 * xs, p1 = s1 * xs;
 #pragma unroll
-          for (int ch = 0; ch < 4; ++ch) {
-            if (ch < nch) {
-              float v0[16], v1[16];
-              const uint32_t col = b * 256u + (uint32_t)(c_lo + ch * 16);
-              tmem_ld16x2(t_lane + col, t_lane + col + 128u, v0, v1);
+            for (int pr = 0; pr < 2; ++pr) {
+              float v0[32], v1[32];
+              const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
+              tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const float xs = sxk[ch * 16 + i];
-                acc0[ch * 16 + i] = fmaf(v0[i], s0 * xs, acc0[ch * 16 + i]);
-                acc1[ch * 16 + i] = fmaf(v1[i], s1 * xs, acc1[ch * 16 + i]);
+              for (int i = 0; i < 32; ++i) {
+                acc0[pr * 32 + i] = fmaf(v0[i], p0, acc0[pr * 32 + i]);
+                acc1[pr * 32 + i] = fmaf(v1[i], p1, acc1[pr * 32 + i]);
+              }
+            }
+          } else {
+            const float* sxk = sxb + k * BN + c_lo;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+              if (pr < npair) {
+                float v0[32], v1[32];
+                const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
+                tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const float xs = sxk[pr * 32 + i];
+                  acc0[pr * 32 + i] = fmaf(v0[i], s0 * xs, acc0[pr * 32 + i]);
+                  acc1[pr * 32 + i] = fmaf(v1[i], s1 * xs, acc1[pr * 32 + i]);
+                }
               }
             }
           }
@@ -439,43 +507,152 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++acc_it;
         }
         if (!ok) break;
-
-        if (split) {
-          // publish this split's partial tile, the last arriving split finishes it
-          const size_t tile = (size_t)(u / p.ksplit);
-          float* mine = p.part + ((tile * p.ksplit + U.q) * 2) * (size_t)BN * BM;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (i < ncols) {
-              mine[(size_t)(c_lo + i) * BM + lrow] = acc0[i];
-              mine[(size_t)(BN + c_lo + i) * BM + lrow] = acc1[i];
-            }
-          }
-          __threadfence();
-          if (!epi_sync()) break;
-          if (etid == 0) *last_flag = (atomicAdd(p.counters + tile, 1) == p.ksplit - 1);
-          if (!epi_sync()) break;
-          if (!*last_flag) continue;
-          __threadfence();
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (i < ncols) {
-              float v0 = 0.0f, v1 = 0.0f;
-              for (int q = 0; q < p.ksplit; ++q) {
-                const float* pq = p.part + ((tile * p.ksplit + q) * 2) * (size_t)BN * BM;
-                v0 += __ldcg(pq + (size_t)(c_lo + i) * BM + lrow);
-                v1 += __ldcg(pq + (size_t)(BN + c_lo + i) * BM + lrow);
-              }
-              acc0[i] = v0;
-              acc1[i] = v1;
-            }
-          }
-          if (etid == 0) p.counters[tile] = 0;
+        mbar_arrive(&sempty[sb]);  // this unit's scales are no longer read
+        ++s_it;
+      } else {
+        // BF16: the accumulator of the whole K range (or this split of it) is in tensor memory
+        const uint32_t b = acc_it & 1u;
+        if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
+          ok = false;
+          break;
         }
+        tc_fence_after_sync();
+#pragma unroll
+        for (int pr = 0; pr < 2; ++pr) {
+          if (pr < npair) {
+            float v0[32], v1[32];
+            const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
+            tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              acc0[pr * 32 + i] = v0[i];
+              acc1[pr * 32 + i] = v1[i];
+            }
+          }
+        }
+        tc_fence_before_sync();
+        mbar_arrive(&tempty[b]);
+        ++acc_it;
+      }
 
+      // element (i) of this thread <-> partial-tile index (row-major per tile of [BN or BM][128])
+      auto pidx = [&](int i) -> size_t {
+        return TM ? (size_t)lrow * 128 + (size_t)(c_lo + i) : (size_t)(c_lo + i) * BM + (size_t)lrow;
+      };
+      if (split) {
+        // publish this split's partial tile; the last arriving split finishes it
+        const size_t tile = (size_t)(u / p.ksplit);
+        float* mine = p.part + ((tile * p.ksplit + U.q) * 2) * (size_t)BN * BM;
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          if (i < ncols) {
+            mine[pidx(i)] = acc0[i];
+            mine[(size_t)BN * BM + pidx(i)] = acc1[i];
+          }
+        }
+        __threadfence();
+        if (!epi_sync()) break;
+        if (etid == 0) *last_flag = (atomicAdd(p.counters + tile, 1) == p.ksplit - 1);
+        if (!epi_sync()) break;
+        const bool last = *last_flag != 0;
+        if (!epi_sync()) break;  // every thread has read last_flag before the next unit writes it
+        if (!last) continue;
+        __threadfence();
+        // sum the splits in split order; the loads of one split are independent of each other
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+          acc0[i] = 0.0f;
+          acc1[i] = 0.0f;
+        }
+        for (int q = 0; q < p.ksplit; ++q) {
+          const float* pq = p.part + ((tile * p.ksplit + q) * 2) * (size_t)BN * BM;
+#pragma unroll
+          for (int i = 0; i < 64; ++i) {
+            if (i < ncols) {
+              acc0[i] += __ldcg(pq + pidx(i));
+              acc1[i] += __ldcg(pq + (size_t)BN * BM + pidx(i));
+            }
+          }
+        }
+        if (etid == 0) p.counters[tile] = 0;
+      }
+
+      // ---- final values of this unit
+      float* redp = red + (size_t)(u_it & 1u) * 512;  // maxima, double-buffered by unit parity
+      if constexpr (TM) {
+        const bool row_ok = lrow < U.nvalid;
+        const size_t row = (size_t)(U.rowB + lrow);
         if constexpr (MODE == MODE_SWIGLU) {
+          // rows past the chunk hold other tokens' data: no SwiGLU, no store
+          if (row_ok) {
+#pragma unroll
+            for (int i = 0; i < 64; ++i) acc0[i] = silu(acc0[i]) * acc1[i];
+          }
+          const size_t col = (size_t)U.j * BM + c_lo;
+          if constexpr (F8) {
+            // e4m3 per 1x128 group: the group is this row's 128 columns of the tile (two halves)
+            float a = 0.0f;
+            if (row_ok) {
+#pragma unroll
+              for (int i = 0; i < 64; ++i) a = fmaxf(a, fabsf(acc0[i]));
+            }
+            redp[half * 128 + lrow] = a;
+            if (!epi_sync()) break;
+            if (row_ok) {
+              const float amax = fmaxf(redp[lrow], redp[128 + lrow]);
+              const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
+              const float inv = 1.0f / sc;  // one division per group; the codes use h * (1/s)
+              uint8_t* dst = static_cast<uint8_t*>(p.out) + row * oc + col;
+#pragma unroll
+              for (int v = 0; v < 4; ++v) {
+                const float* h = acc0 + 16 * v;
+                uint4 w;
+                w.x = pack_e4m3x4(h[0] * inv, h[1] * inv, h[2] * inv, h[3] * inv);
+                w.y = pack_e4m3x4(h[4] * inv, h[5] * inv, h[6] * inv, h[7] * inv);
+                w.z = pack_e4m3x4(h[8] * inv, h[9] * inv, h[10] * inv, h[11] * inv);
+                w.w = pack_e4m3x4(h[12] * inv, h[13] * inv, h[14] * inv, h[15] * inv);
+                reinterpret_cast<uint4*>(dst)[v] = w;
+              }
+              if (half == 0) p.out_scales[row * (oc / 128) + U.j] = sc;
+            }
+          } else {
+            if (row_ok) {
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * oc + col);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                dst[v] = make_uint4(pack_bf16x2(acc0[8 * v + 0], acc0[8 * v + 1]),
+                                    pack_bf16x2(acc0[8 * v + 2], acc0[8 * v + 3]),
+                                    pack_bf16x2(acc0[8 * v + 4], acc0[8 * v + 5]),
+                                    pack_bf16x2(acc0[8 * v + 6], acc0[8 * v + 7]));
+            }
+          }
+        } else {
+          if (row_ok) {
+            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.out) + row * oc;
+            uint4* d0 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * p.pair_stride + c_lo);
+#pragma unroll
+            for (int v = 0; v < 8; ++v)
+              d0[v] = make_uint4(pack_bf16x2(acc0[8 * v + 0], acc0[8 * v + 1]),
+                                 pack_bf16x2(acc0[8 * v + 2], acc0[8 * v + 3]),
+                                 pack_bf16x2(acc0[8 * v + 4], acc0[8 * v + 5]),
+                                 pack_bf16x2(acc0[8 * v + 6], acc0[8 * v + 7]));
+            if (U.a1) {
+              uint4* d1 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * p.pair_stride + BM + c_lo);
+#pragma unroll
+              for (int v = 0; v < 8; ++v)
+                d1[v] = make_uint4(pack_bf16x2(acc1[8 * v + 0], acc1[8 * v + 1]),
+                                   pack_bf16x2(acc1[8 * v + 2], acc1[8 * v + 3]),
+                                   pack_bf16x2(acc1[8 * v + 4], acc1[8 * v + 5]),
+                                   pack_bf16x2(acc1[8 * v + 6], acc1[8 * v + 7]));
+            }
+          }
+        }
+      } else {
+        // weight-major: this thread holds output column (weight row) col0 for token columns c_lo + i
+        const int col0 = (MODE == MODE_SWIGLU) ? U.j * BM + lrow : U.j * p.pair_stride + lrow;
+        if constexpr (MODE == MODE_SWIGLU && F8) {
           // h = silu(g) * u, then e4m3 per 1x128 group: the group is this tile's 128 rows
-          float* redh = red + half * 4 * 64;
+          float* redh = redp + half * 256;  // [4 quarters][64 columns]
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             if (i < ncols) {
@@ -493,73 +670,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             if (i < ncols) {
-              const float amax =
-                  fmaxf(fmaxf(redh[i], redh[64 + i]), fmaxf(redh[128 + i], redh[192 + i]));
+              const float amax = fmaxf(fmaxf(redh[i], redh[64 + i]), fmaxf(redh[128 + i], redh[192 + i]));
               const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
               const size_t row = (size_t)(U.rowB + c_lo + i);
-              const __nv_fp8_storage_t code = __nv_cvt_float_to_fp8(__fdiv_rn(acc0[i], sc), __NV_SATFINITE, __NV_E4M3);
-              hq[row * oc + col0] = code;
+              hq[row * oc + col0] = __nv_cvt_float_to_fp8(__fdividef(acc0[i], sc), __NV_SATFINITE, __NV_E4M3);
               if (quarter == 0 && lane == 0) p.out_scales[row * G + U.j] = sc;
             }
           }
-          if (!half_sync(half)) break;  // the maxima are read before the next unit writes them
         } else {
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
-          for (int i = 0; i < 64; ++i)
-            if (i < ncols) finish(c_lo + i, acc0[i], acc1[i]);
-        }
-      } else {
-        // BF16: the accumulator of the whole K range (or this split of it) is in tensor memory
-        const uint32_t b = acc_it & 1u;
-        if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after_sync();
-        const size_t tile = (size_t)(u / p.ksplit);
-        float* mine = split ? p.part + ((tile * p.ksplit + U.q) * 2) * (size_t)BN * BM : nullptr;
-#pragma unroll
-        for (int ch = 0; ch < 4; ++ch) {
-          if (ch < nch) {
-            float v0[16], v1[16];
-            const uint32_t col = b * 256u + (uint32_t)(c_lo + ch * 16);
-            tmem_ld16x2(t_lane + col, t_lane + col + 128u, v0, v1);
-#pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int c = c_lo + ch * 16 + i;
-              if (c < U.nvalid) {
-                if (split) {
-                  mine[(size_t)c * BM + lrow] = v0[i];
-                  mine[(size_t)(BN + c) * BM + lrow] = v1[i];
-                } else {
-                  finish(c, v0[i], v1[i]);
-                }
+          for (int i = 0; i < 64; ++i) {
+            if (i < ncols) {
+              const size_t row = (size_t)(U.rowB + c_lo + i);
+              if constexpr (MODE == MODE_SWIGLU) {
+                o[row * oc + col0] = __float2bfloat16_rn(silu(acc0[i]) * acc1[i]);
+              } else {
+                o[row * oc + col0] = __float2bfloat16_rn(acc0[i]);
+                if (U.a1) o[row * oc + col0 + BM] = __float2bfloat16_rn(acc1[i]);
               }
             }
           }
-        }
-        tc_fence_before_sync();
-        mbar_arrive(&tempty[b]);
-        ++acc_it;
-        if (split) {
-          __threadfence();
-          if (!epi_sync()) break;
-          if (etid == 0) *last_flag = (atomicAdd(p.counters + tile, 1) == p.ksplit - 1);
-          if (!epi_sync()) break;
-          if (*last_flag) {
-            __threadfence();
-            for (int i = 0; i < ncols; ++i) {
-              float v0 = 0.0f, v1 = 0.0f;
-              for (int q = 0; q < p.ksplit; ++q) {
-                const float* pq = p.part + ((tile * p.ksplit + q) * 2) * (size_t)BN * BM;
-                v0 += __ldcg(pq + (size_t)(c_lo + i) * BM + lrow);
-                v1 += __ldcg(pq + (size_t)(BN + c_lo + i) * BM + lrow);
-              }
-              finish(c_lo + i, v0, v1);
-            }
-            if (etid == 0) p.counters[tile] = 0;
-          }
-          if (!epi_sync()) break;  // last_flag is read before the next unit overwrites it
         }
       }
     }
@@ -580,6 +711,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 struct Plan {
   int ksplit, kb_per_split, kb_total, stages, nslots, pairs;
+  bool tm;
   size_t smem;
   uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
   size_t part_bytes, counter_bytes;
@@ -594,6 +726,9 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   pl.kb_total = K * esz / ROW_BYTES;
   pl.nslots = p.P + p.has_shared;
   pl.pairs = (mode == MODE_SWIGLU) ? p.I / BM : (NA + 2 * BM - 1) / (2 * BM);
+  // token-major when an expert is expected to hold enough rows to fill a 128-row MMA
+  const double rows_per_slot = (double)p.T * p.K / std::max(1, p.P);
+  pl.tm = rows_per_slot >= 64.0;
   // upper bound of the token chunks over all slots
   long chunks;
   if (p.layout == MOE_LAYOUT_MASKED) {
@@ -630,18 +765,18 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
     extra += bytes;
     return off;
   };
-  // reserve stage space first, assume the maximum; offsets of the rest follow the stages
-  const size_t sx_b = f8 ? (size_t)pl.kb_per_split * BN * 4 : 0;
-  const size_t sw_b = f8 ? (size_t)2 * pl.kb_per_split * 4 : 0;
-  const size_t red_b = (f8 && mode == MODE_SWIGLU) ? 2 * 4 * 64 * 4 : 0;
+  const size_t sx_b = f8 ? (size_t)2 * pl.kb_per_split * BN * 4 : 0;
+  const size_t sw_b = f8 ? (size_t)2 * 2 * pl.kb_per_split * 4 : 0;
+  const size_t red_b = (size_t)2 * 512 * 4;
   const size_t pre_b = (size_t)(pl.nslots + 1) * 4;
+  pl.stages = 0;
   for (int st = 6; st >= 2; --st) {
     extra = (size_t)st * STAGE_BYTES;
     pl.sx_off = (uint32_t)carve(sx_b, 16);
     pl.sw_off = (uint32_t)carve(sw_b, 16);
     pl.red_off = (uint32_t)carve(red_b, 16);
     pl.pre_off = (uint32_t)carve(pre_b, 16);
-    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 8) * 8, 8);
+    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 12) * 8, 8);
     pl.misc_off = (uint32_t)carve(16, 16);
     const size_t total = extra + 1024;
     if ((int)total <= smem_cap) {
@@ -655,23 +790,23 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   return pl;
 }
 
-template <bool F8, int MODE>
+template <bool F8, int MODE, bool TM>
 int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float* act_scales, const void* w,
               const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
               int32_t* err, void* ws, cudaStream_t st) {
   const DeviceInfo& di = device_info();
-  static bool attr_set[2][2][64] = {};
+  static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  auto kern = grouped_gemm_tc_kernel<F8, MODE>;
-  if (dev < 64 && !attr_set[F8][MODE][dev]) {
+  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM>;
+  if (dev < 64 && !attr_set[dev]) {
     // the register split above must fit in what the launch provides, or setmaxnreg.inc would wait forever
     cudaFuncAttributes fa{};
     if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return MOE_ERR_CUDA;
-    if (fa.numRegs * NUM_THREADS < REGS_NEEDED) return MOE_ERR_UNSUPPORTED;
+    if (fa.numRegs * NUM_THREADS < Regs<F8>::needed) return MOE_ERR_UNSUPPORTED;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin) != cudaSuccess)
       return MOE_ERR_CUDA;
-    attr_set[F8][MODE][dev] = true;
+    attr_set[dev] = true;
   }
   const int esz = F8 ? 1 : 2;
   const CUtensorMapDataType dt = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
@@ -819,17 +954,24 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
   const Plan pl = make_plan(p, mode, di.sm_count, di.max_smem_optin);
   if (pl.stages == 0) return MOE_ERR_UNSUPPORTED;
   const bool f8 = p.wt == MOE_E4M3;
-  if (f8 && mode == MODE_SWIGLU)
-    return launch_tc<true, MODE_SWIGLU>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales,
-                                        err, ws, st);
-  if (f8)
-    return launch_tc<true, MODE_DOWN>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err,
-                                      ws, st);
-  if (mode == MODE_SWIGLU)
-    return launch_tc<false, MODE_SWIGLU>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales,
-                                         err, ws, st);
-  return launch_tc<false, MODE_DOWN>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err,
-                                     ws, st);
+#define MOE_LAUNCH(F8_, MODE_, TM_)                                                                              \
+  return launch_tc<F8_, MODE_, TM_>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err, \
+                                    ws, st)
+  if (f8) {
+    if (mode == MODE_SWIGLU) {
+      if (pl.tm) MOE_LAUNCH(true, MODE_SWIGLU, true);
+      MOE_LAUNCH(true, MODE_SWIGLU, false);
+    }
+    if (pl.tm) MOE_LAUNCH(true, MODE_DOWN, true);
+    MOE_LAUNCH(true, MODE_DOWN, false);
+  }
+  if (mode == MODE_SWIGLU) {
+    if (pl.tm) MOE_LAUNCH(false, MODE_SWIGLU, true);
+    MOE_LAUNCH(false, MODE_SWIGLU, false);
+  }
+  if (pl.tm) MOE_LAUNCH(false, MODE_DOWN, true);
+  MOE_LAUNCH(false, MODE_DOWN, false);
+#undef MOE_LAUNCH
 }
 
 }  // namespace moe

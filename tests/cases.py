@@ -15,4 +15,10 @@ SMALL = {
         name="e4m3_eplb_zipf", T=48, H=256, I=384, E=16, K=4, M_max=48, redundant=4),
     "e4m3_contig": CONFIGS["prefill"].replace(
         name="e4m3_contig", T=64, H=256, I=256, E=32, K=4),
+    # >= 64 expected rows per expert: the token-major GEMM orientation, experts
+    # above 128 rows split into near-equal chunks
+    "e4m3_contig_tm": CONFIGS["prefill"].replace(
+        name="e4m3_contig_tm", T=320, H=384, I=256, E=5, K=2),
+    "bf16_masked_tm": CONFIGS["mixtral_decode"].replace(
+        name="bf16_masked_tm", T=200, H=256, I=384, E=4, K=2, M_max=200),
 }
