@@ -98,16 +98,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 
 // Wait for the phase of `bar` with the given parity to complete.  Gives up
 // (returns false) when *abort is set by another role of the CTA, or after
-// `timeout_ns` of global time, in which case it sets *abort itself.
+// `timeout_cycles` SM clock cycles, in which case it sets *abort itself.
+// The clock is read only every 64 polls, so a wait that ends quickly costs
+// nothing beyond the polls themselves.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
-                                          uint64_t timeout_ns) {
+                                          long long timeout_cycles) {
   if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = global_timer_ns();
+  long long t0 = 0;
   uint32_t n = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if ((++n & 31u) == 0) {
+    if ((++n & 63u) == 0) {
       if (*abort) return false;
-      if (global_timer_ns() - t0 > timeout_ns) {
+      const long long now = clock64();
+      if (t0 == 0) {
+        t0 = now;
+      } else if (now - t0 > timeout_cycles) {
         *abort = 1;
         return false;
       }
@@ -140,6 +145,13 @@ __device__ __forceinline__ void tma_load_2d_hint(void* smem_dst, const CUtensorM
       "{%3, %4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y), "l"(policy)
       : "memory");
+}
+
+// Prefetch a 2-D tile into L2 (no shared memory, no completion tracking).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap* map, int32_t x, int32_t y) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(reinterpret_cast<uint64_t>(map)),
+               "r"(x), "r"(y)
+               : "memory");
 }
 
 __device__ __forceinline__ uint64_t policy_evict_first() {

@@ -18,20 +18,20 @@
 //     up tile (same rows of W3).  Down: two consecutive 128-row tiles of W2.
 //     Units exist only for chunks with rows: each CTA builds the unit list from
 //     masked_m on the device at kernel start.
-//   * Two orientations, chosen per launch from the problem's expected rows per
-//     expert:
-//       - weight-major (decode): the weight tile is the MMA's M = 128 side and
-//         the chunk's tokens its N side, rounded up to 16 -- a decode expert
-//         with a few tokens streams its weights at full width and issues N = 16
-//         MMAs;
-//       - token-major (prefill): the 128 token rows are the M side and the gate
-//         and up tiles together one N = 256 MMA; the activation scale becomes
-//         one value per thread and the SwiGLU and the stores are row-local.
+//   * Two orientations:
+//       - token-major (every FP8 problem, and BF16 prefill): the 128 token rows
+//         are the MMA's M side and the gate and up tiles together one N = 256
+//         MMA; the activation scale is one value per thread, and the SwiGLU, the
+//         e4m3 re-quantisation of h and the stores are row-local;
+//       - weight-major (BF16 decode): the weight tile is the M = 128 side and the
+//         chunk's tokens the N side, rounded up to 16 -- an expert with a few
+//         tokens streams its weights at full width and issues N = 16 MMAs.
 //   * Warp 0: TMA producer (weights with an evict-first L2 hint).  Warp 1:
 //     tensor-memory allocator and the single MMA-issuing thread.  Warps 2-3:
-//     FP8 scale loaders (a unit's activation and weight scales into a double
-//     buffer in shared memory).  Warps 4-11: epilogue, two warps per
-//     tensor-memory lane quarter.
+//     FP8 scale loaders (the activation and weight scales of each K block into
+//     an 8-slot ring in shared memory, ahead of the epilogue; keeping the
+//     scales out of the stages leaves room for four 48 KB stages).  Warps 4-11:
+//     epilogue, two warps per tensor-memory lane quarter.
 //   * FP8: the MMAs of one 128-K block write one of two tensor-memory buffers;
 //     the epilogue reads it, scales it and adds it into fp32 registers while
 //     the MMA fills the other.  BF16: the whole K range accumulates in tensor
@@ -56,8 +56,10 @@ constexpr int STAGE_BYTES = 2 * TILE_A_BYTES + TILE_B_BYTES;  // weight tile 0 |
 constexpr int NUM_THREADS = 384;    // three warpgroups
 constexpr int EPI_THREADS = 256;    // warpgroups 1 and 2
 constexpr int EPI_WARP0 = 4;
+constexpr int EPI_WARPS = EPI_THREADS / 32;  // epilogue barriers take one arrival per warp
 constexpr int LOAD_WARP0 = 2;       // warps 2 and 3 load FP8 scales
 constexpr int LOAD_THREADS = 64;
+constexpr int RING = 8;             // K blocks of scales staged ahead of the epilogue
 // Register split (setmaxnreg): warpgroup 0 (TMA, MMA, scale loads) gives
 // registers to the two epilogue warpgroups, which hold 2 x 64 fp32
 // accumulators per thread.  4*32*ctrl + 8*32*epi must not exceed
@@ -69,7 +71,8 @@ struct Regs {
   static constexpr int needed = 4 * 32 * ctrl + 8 * 32 * epi;
 };
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint64_t TIMEOUT_NS = 2000000000ull;
+// Bound of every wait: 4e9 SM cycles, about 2 s at the 2.07 GHz maximum clock.
+constexpr long long TIMEOUT = 4000000000LL;
 
 struct TcParams {
   int nslots, masked, M_max;
@@ -156,22 +159,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
                            const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
                            const __grid_constant__ CUtensorMap tmB128, const TcParams p) {
+  static_assert(TM || !F8, "FP8 runs token-major");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
-  const int KBS = p.kb_per_split;
-  float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [2 bufs][KBS][BN] activation scales, [k][row]
-  float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [2 bufs][2 tiles][KBS] weight scales
+  float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [RING][BN] activation scales of one K block
+  float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [RING][2 tiles] weight scales of one K block
   float* red = reinterpret_cast<float*>(smem + p.red_off);  // [2 parities][512] group maxima
   int* prefix = reinterpret_cast<int*>(smem + p.pre_off);   // [nslots + 1] unit prefix
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* tfull = empty + p.stages;  // [2] accumulator buffer written
   uint64_t* tempty = tfull + 2;        // [2] accumulator buffer read
-  uint64_t* sfull = tempty + 2;        // [2] scale buffer loaded
-  uint64_t* sempty = sfull + 2;        // [2] scale buffer consumed
-  uint64_t* drain = sempty + 2;        // [1]
+  uint64_t* rfull = tempty + 2;        // [RING] scale slot loaded
+  uint64_t* rempty = rfull + RING;     // [RING] scale slot consumed
+  uint64_t* drain = rempty + RING;     // [1]
   uint64_t* ebar = drain + 1;          // [1] all epilogue threads
-  uint64_t* hbar = ebar + 1;           // [2] the 128 epilogue threads of one column half
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + p.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
   int* last_flag = reinterpret_cast<int*>(smem + p.misc_off + 8);
@@ -186,13 +188,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], EPI_THREADS);
-      mbar_init(&sfull[i], LOAD_THREADS);
-      mbar_init(&sempty[i], EPI_THREADS);
-      mbar_init(&hbar[i], 128);
+      mbar_init(&tempty[i], EPI_WARPS);
+    }
+    for (int i = 0; i < RING; ++i) {
+      mbar_init(&rfull[i], LOAD_THREADS);
+      mbar_init(&rempty[i], EPI_WARPS);
     }
     mbar_init(drain, 1);
-    mbar_init(ebar, EPI_THREADS);
+    mbar_init(ebar, EPI_WARPS);
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           const uint32_t bytes = TILE_A_BYTES * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
           for (int kb = U.kb0; kb < U.kb1; ++kb) {
-            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT_NS)) {
+            if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT)) {
               ok = false;
               break;
             }
@@ -286,8 +289,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (long i = first; i < issued; ++i) {
             const int st = (int)(i % p.stages);
             const uint32_t ph = (uint32_t)((i / p.stages) & 1);
-            const uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(&full[st], ph) && global_timer_ns() - t0 < TIMEOUT_NS) {
+            const long long t0 = clock64();
+            while (!mbar_try_wait(&full[st], ph) && clock64() - t0 < TIMEOUT) {
             }
           }
         }
@@ -309,7 +312,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t b = 0;
           if constexpr (!F8) {
             b = acc_it & 1u;
-            if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
+            if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
               ok = false;
               break;
             }
@@ -318,12 +321,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           for (int kb = U.kb0; kb < U.kb1; ++kb) {
             if constexpr (F8) {
               b = acc_it & 1u;
-              if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) {
+              if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
                 ok = false;
                 break;
               }
             }
-            if (!mbar_wait(&full[stage], phase, abort_flag, TIMEOUT_NS)) {
+            if (!mbar_wait(&full[stage], phase, abort_flag, TIMEOUT)) {
               ok = false;
               break;
             }
@@ -364,56 +367,58 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok && any) {
           // all MMAs issued by this thread must finish before tensor memory is freed
           tc_commit(drain);
-          const uint64_t t0 = global_timer_ns();
-          while (!mbar_try_wait(drain, 0) && global_timer_ns() - t0 < TIMEOUT_NS) {
+          const long long t0 = clock64();
+          while (!mbar_try_wait(drain, 0) && clock64() - t0 < TIMEOUT) {
           }
         }
       }
     } else if (F8) {
       // ------------------------------------------------------------ FP8 scale loaders
+      // Fill the scale ring K block by K block, four blocks per pass: one thread per token
+      // row reads the row's four scales with one 16-byte load (or four scalar loads).
       const int lt = tid - LOAD_WARP0 * 32;
-      uint32_t it = 0;
-      for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+      uint32_t g = 0;  // K blocks staged so far
+      bool ok = true;
+      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
         const Unit U = decode_unit<MODE>(p, prefix, u);
-        const uint32_t sb = it & 1u;
-        if (!mbar_wait(&sempty[sb], ((it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT_NS)) break;
-        const int n = U.nvalid, nkb = U.kb1 - U.kb0;
-        float* sxb = sx + (size_t)sb * KBS * BN;
-        // one thread per token row: its nkb scales are contiguous in global memory; read them
-        // with independent 16-byte loads, store them transposed ([k][row], conflict-free)
-        for (int c = lt; c < n; c += LOAD_THREADS) {
-          const float* src = p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + U.kb0;
-          if ((reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-            constexpr int VB = 4;
-            for (int k0 = 0; k0 < nkb; k0 += 4 * VB) {
-              float4 v[VB];
-#pragma unroll
-              for (int b = 0; b < VB; ++b)
-                if (k0 + 4 * b + 3 < nkb) v[b] = __ldg(reinterpret_cast<const float4*>(src + k0 + 4 * b));
-#pragma unroll
-              for (int b = 0; b < VB; ++b) {
-                const int k = k0 + 4 * b;
-                if (k + 3 < nkb) {
-                  sxb[(k + 0) * BN + c] = v[b].x;
-                  sxb[(k + 1) * BN + c] = v[b].y;
-                  sxb[(k + 2) * BN + c] = v[b].z;
-                  sxb[(k + 3) * BN + c] = v[b].w;
-                } else {
-                  for (int kk = k; kk < nkb && kk < k + 4; ++kk) sxb[kk * BN + c] = __ldg(src + kk);
-                }
-              }
-            }
-          } else {
-            for (int k = 0; k < nkb; ++k) sxb[k * BN + c] = __ldg(src + k);
-          }
-        }
-        float* swb = sw + (size_t)sb * 2 * KBS;
         const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
-        for (int k = lt; k < nkb; k += LOAD_THREADS) {
-          swb[k] = __ldg(p.a_scales + (size_t)ra0 * p.scale_cols + U.kb0 + k);
-          swb[KBS + k] = U.a1 ? __ldg(p.a_scales + (size_t)ra1 * p.scale_cols + U.kb0 + k) : 0.0f;
+        for (int k0 = U.kb0; ok && k0 < U.kb1; k0 += 4) {
+          const int nk = min(4, U.kb1 - k0);
+          for (int j = 0; j < nk; ++j) {
+            const uint32_t gj = g + j;
+            if (!mbar_wait(&rempty[gj % RING], ((gj / RING) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
+              ok = false;
+              break;
+            }
+          }
+          if (!ok) break;
+          for (int c = lt; c < U.nvalid; c += LOAD_THREADS) {
+            const float* src = p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + k0;
+            float v[4];
+            if (nk == 4 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
+              const float4 f = __ldg(reinterpret_cast<const float4*>(src));
+              v[0] = f.x;
+              v[1] = f.y;
+              v[2] = f.z;
+              v[3] = f.w;
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) v[j] = (j < nk) ? __ldg(src + j) : 0.0f;
+            }
+#pragma unroll
+            for (int j = 0; j < 4; ++j)
+              if (j < nk) sx[((g + j) % RING) * BN + c] = v[j];
+          }
+          if (lt < 2 * nk) {
+            const int j = lt >> 1, t = lt & 1;
+            float w = 0.0f;
+            if (t == 0) w = __ldg(p.a_scales + (size_t)ra0 * p.scale_cols + k0 + j);
+            else if (U.a1) w = __ldg(p.a_scales + (size_t)ra1 * p.scale_cols + k0 + j);
+            sw[((g + j) % RING) * 2 + t] = w;
+          }
+          for (int j = 0; j < nk; ++j) mbar_arrive(&rfull[(g + j) % RING]);
+          g += nk;
         }
-        mbar_arrive(&sfull[sb]);
       }
     }
   } else {
@@ -424,22 +429,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = (warp - EPI_WARP0) >> 2; // column half (warpgroup 1 or 2)
     const int lrow = quarter * 32 + lane;     // tensor-memory lane of this thread
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    uint32_t acc_it = 0, s_it = 0, u_it = 0;
+    uint32_t acc_it = 0, r_it = 0, u_it = 0;
     uint32_t ephase = 0;
-    uint32_t hphase[2] = {0, 0};
     bool ok = true;
     const size_t oc = (size_t)p.out_cols;
+    // one arrival per warp, after the warp's own threads are ordered by __syncwarp
+    auto warp_arrive = [&](uint64_t* bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
     // bounded barriers among the epilogue threads (a plain bar.sync could not give up)
     auto epi_sync = [&]() {
-      mbar_arrive(ebar);
-      const bool r = mbar_wait(ebar, ephase, abort_flag, TIMEOUT_NS);
+      warp_arrive(ebar);
+      const bool r = mbar_wait(ebar, ephase, abort_flag, TIMEOUT);
       ephase ^= 1u;
-      return r;
-    };
-    auto half_sync = [&](int h) {
-      mbar_arrive(&hbar[h]);
-      const bool r = mbar_wait(&hbar[h], hphase[h], abort_flag, TIMEOUT_NS);
-      hphase[h] ^= 1u;
       return r;
     };
     for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++u_it) {
@@ -459,60 +462,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
 
       if constexpr (F8) {
-        const uint32_t sb = s_it & 1u;
-        if (!mbar_wait(&sfull[sb], (s_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) break;
-        const float* sxb = sx + (size_t)sb * KBS * BN;
-        const float* swb = sw + (size_t)sb * 2 * KBS;
         for (int k = 0; k < nkb; ++k) {
+          const uint32_t slot = r_it % RING;
+          if (!mbar_wait(&rfull[slot], (r_it / RING) & 1u, abort_flag, TIMEOUT)) {
+            ok = false;
+            break;
+          }
           const uint32_t b = acc_it & 1u;
-          if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
+          if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT)) {
             ok = false;
             break;
           }
           tc_fence_after_sync();
-          const float s0 = swb[k], s1 = swb[KBS + k];
+          const float* sxs = sx + slot * BN;
+          const float s0 = sw[slot * 2], s1 = sw[slot * 2 + 1];
           if constexpr (TM) {
-            const float xs = sxb[k * BN + lrow];
+            const float xs = sxs[lrow];
             const float p0 = s0 * xs, p1 = s1 * xs;
 #pragma unroll
             for (int pr = 0; pr < 2; ++pr) {
               float v0[32], v1[32];
               const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
               tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
+              if (pr == 1) {  // the buffer is read: hand it back before the last multiply-adds
+                tc_fence_before_sync();
+                warp_arrive(&tempty[b]);
+              }
 #pragma unroll
               for (int i = 0; i < 32; ++i) {
                 acc0[pr * 32 + i] = fmaf(v0[i], p0, acc0[pr * 32 + i]);
                 acc1[pr * 32 + i] = fmaf(v1[i], p1, acc1[pr * 32 + i]);
               }
             }
-          } else {
-            const float* sxk = sxb + k * BN + c_lo;
-#pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-              if (pr < npair) {
-                float v0[32], v1[32];
-                const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
-                tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                  const float xs = sxk[pr * 32 + i];
-                  acc0[pr * 32 + i] = fmaf(v0[i], s0 * xs, acc0[pr * 32 + i]);
-                  acc1[pr * 32 + i] = fmaf(v1[i], s1 * xs, acc1[pr * 32 + i]);
-                }
-              }
-            }
           }
-          tc_fence_before_sync();
-          mbar_arrive(&tempty[b]);
+          warp_arrive(&rempty[slot]);  // this block's scales are no longer read
+          ++r_it;
           ++acc_it;
         }
         if (!ok) break;
-        mbar_arrive(&sempty[sb]);  // this unit's scales are no longer read
-        ++s_it;
       } else {
         // BF16: the accumulator of the whole K range (or this split of it) is in tensor memory
         const uint32_t b = acc_it & 1u;
-        if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT_NS)) {
+        if (!mbar_wait(&tfull[b], (acc_it >> 1) & 1u, abort_flag, TIMEOUT)) {
           ok = false;
           break;
         }
@@ -531,7 +522,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         tc_fence_before_sync();
-        mbar_arrive(&tempty[b]);
+        warp_arrive(&tempty[b]);
         ++acc_it;
       }
 
@@ -650,34 +641,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // weight-major: this thread holds output column (weight row) col0 for token columns c_lo + i
         const int col0 = (MODE == MODE_SWIGLU) ? U.j * BM + lrow : U.j * p.pair_stride + lrow;
-        if constexpr (MODE == MODE_SWIGLU && F8) {
-          // h = silu(g) * u, then e4m3 per 1x128 group: the group is this tile's 128 rows
-          float* redh = redp + half * 256;  // [4 quarters][64 columns]
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (i < ncols) {
-              const float h = silu(acc0[i]) * acc1[i];
-              acc0[i] = h;
-              float a = fabsf(h);
-#pragma unroll
-              for (int off = 16; off > 0; off >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, off));
-              if (lane == 0) redh[quarter * 64 + i] = a;
-            }
-          }
-          if (!half_sync(half)) break;
-          uint8_t* hq = static_cast<uint8_t*>(p.out);
-          const int G = p.out_cols / 128;
-#pragma unroll
-          for (int i = 0; i < 64; ++i) {
-            if (i < ncols) {
-              const float amax = fmaxf(fmaxf(redh[i], redh[64 + i]), fmaxf(redh[128 + i], redh[192 + i]));
-              const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
-              const size_t row = (size_t)(U.rowB + c_lo + i);
-              hq[row * oc + col0] = __nv_cvt_float_to_fp8(__fdividef(acc0[i], sc), __NV_SATFINITE, __NV_E4M3);
-              if (quarter == 0 && lane == 0) p.out_scales[row * G + U.j] = sc;
-            }
-          }
-        } else {
+        {
           __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
@@ -726,9 +690,12 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   pl.kb_total = K * esz / ROW_BYTES;
   pl.nslots = p.P + p.has_shared;
   pl.pairs = (mode == MODE_SWIGLU) ? p.I / BM : (NA + 2 * BM - 1) / (2 * BM);
-  // token-major when an expert is expected to hold enough rows to fill a 128-row MMA
+  // Token-major for FP8 always: the activation scale is then one value per thread and the
+  // SwiGLU / e4m3 re-quantisation of h are row-local, which measured faster than the
+  // weight-major epilogue even for decode experts with a few tokens.  BF16 needs no
+  // promotion; there weight-major is kept for decode-sized experts.
   const double rows_per_slot = (double)p.T * p.K / std::max(1, p.P);
-  pl.tm = rows_per_slot >= 64.0;
+  pl.tm = f8 || rows_per_slot >= 64.0;
   // upper bound of the token chunks over all slots
   long chunks;
   if (p.layout == MOE_LAYOUT_MASKED) {
@@ -765,8 +732,8 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
     extra += bytes;
     return off;
   };
-  const size_t sx_b = f8 ? (size_t)2 * pl.kb_per_split * BN * 4 : 0;
-  const size_t sw_b = f8 ? (size_t)2 * 2 * pl.kb_per_split * 4 : 0;
+  const size_t sx_b = f8 ? (size_t)RING * BN * 4 : 0;
+  const size_t sw_b = f8 ? (size_t)RING * 2 * 4 : 0;
   const size_t red_b = (size_t)2 * 512 * 4;
   const size_t pre_b = (size_t)(pl.nslots + 1) * 4;
   pl.stages = 0;
@@ -776,7 +743,7 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
     pl.sw_off = (uint32_t)carve(sw_b, 16);
     pl.red_off = (uint32_t)carve(red_b, 16);
     pl.pre_off = (uint32_t)carve(pre_b, 16);
-    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 12) * 8, 8);
+    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 2 * RING + 8) * 8, 8);
     pl.misc_off = (uint32_t)carve(16, 16);
     const size_t total = extra + 1024;
     if ((int)total <= smem_cap) {
@@ -958,12 +925,8 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
   return launch_tc<F8_, MODE_, TM_>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err, \
                                     ws, st)
   if (f8) {
-    if (mode == MODE_SWIGLU) {
-      if (pl.tm) MOE_LAUNCH(true, MODE_SWIGLU, true);
-      MOE_LAUNCH(true, MODE_SWIGLU, false);
-    }
-    if (pl.tm) MOE_LAUNCH(true, MODE_DOWN, true);
-    MOE_LAUNCH(true, MODE_DOWN, false);
+    if (mode == MODE_SWIGLU) MOE_LAUNCH(true, MODE_SWIGLU, true);
+    MOE_LAUNCH(true, MODE_DOWN, true);
   }
   if (mode == MODE_SWIGLU) {
     if (pl.tm) MOE_LAUNCH(false, MODE_SWIGLU, true);
