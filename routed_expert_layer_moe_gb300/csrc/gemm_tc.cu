@@ -92,8 +92,8 @@ struct TcParams {
   const float* b_scales;  // activation group scales [rows][K/128]
   void* out;
   float* out_scales;      // e4m3 gate/up output scales [rows][I/128]
-  float* part;            // split-K partial tiles
-  int32_t* counters;      // split-K arrival counters (zero between calls)
+  float* part;            // split-K partial sums [ksplit][rows_total][out_cols] fp32
+  long rows_total;        // rows of the grouped buffers
   int32_t* err;
   uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
 };
@@ -176,7 +176,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* ebar = drain + 1;          // [1] all epilogue threads
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + p.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
-  int* last_flag = reinterpret_cast<int*>(smem + p.misc_off + 8);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
@@ -526,46 +525,34 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++acc_it;
       }
 
-      // element (i) of this thread <-> partial-tile index (row-major per tile of [BN or BM][128])
-      auto pidx = [&](int i) -> size_t {
-        return TM ? (size_t)lrow * 128 + (size_t)(c_lo + i) : (size_t)(c_lo + i) * BM + (size_t)lrow;
-      };
       if (split) {
-        // publish this split's partial tile; the last arriving split finishes it
-        const size_t tile = (size_t)(u / p.ksplit);
-        float* mine = p.part + ((tile * p.ksplit + U.q) * 2) * (size_t)BN * BM;
+        // this split's fp32 partial sums go to the dense [split][row][column] workspace; a
+        // separate reduction kernel adds the splits in split order (no atomics, no waits)
+        float* pq = p.part + (size_t)U.q * p.rows_total * oc;
+        if constexpr (TM) {
+          if (lrow < U.nvalid) {
+            float* prow = pq + (size_t)(U.rowB + lrow) * oc + (size_t)U.j * p.pair_stride + c_lo;
 #pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          if (i < ncols) {
-            mine[pidx(i)] = acc0[i];
-            mine[(size_t)BN * BM + pidx(i)] = acc1[i];
+            for (int v = 0; v < 16; ++v) {
+              reinterpret_cast<float4*>(prow)[v] =
+                  make_float4(acc0[4 * v], acc0[4 * v + 1], acc0[4 * v + 2], acc0[4 * v + 3]);
+              if (U.a1)
+                reinterpret_cast<float4*>(prow + BM)[v] =
+                    make_float4(acc1[4 * v], acc1[4 * v + 1], acc1[4 * v + 2], acc1[4 * v + 3]);
+            }
           }
-        }
-        __threadfence();
-        if (!epi_sync()) break;
-        if (etid == 0) *last_flag = (atomicAdd(p.counters + tile, 1) == p.ksplit - 1);
-        if (!epi_sync()) break;
-        const bool last = *last_flag != 0;
-        if (!epi_sync()) break;  // every thread has read last_flag before the next unit writes it
-        if (!last) continue;
-        __threadfence();
-        // sum the splits in split order; the loads of one split are independent of each other
-#pragma unroll
-        for (int i = 0; i < 64; ++i) {
-          acc0[i] = 0.0f;
-          acc1[i] = 0.0f;
-        }
-        for (int q = 0; q < p.ksplit; ++q) {
-          const float* pq = p.part + ((tile * p.ksplit + q) * 2) * (size_t)BN * BM;
+        } else {
+          const size_t col0 = (size_t)U.j * p.pair_stride + lrow;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             if (i < ncols) {
-              acc0[i] += __ldcg(pq + pidx(i));
-              acc1[i] += __ldcg(pq + (size_t)BN * BM + pidx(i));
+              float* prow = pq + (size_t)(U.rowB + c_lo + i) * oc;
+              prow[col0] = acc0[i];
+              if (U.a1) prow[col0 + BM] = acc1[i];
             }
           }
         }
-        if (etid == 0) p.counters[tile] = 0;
+        continue;
       }
 
       // ---- final values of this unit
@@ -669,6 +656,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (tid == 0 && *abort_flag) atomicOr(p.err, MOE_FLAG_TIMEOUT);
 }
 
+// Split-K: out[row][col] = bf16(sum over splits q = 0..ksplit-1, in order, of part[q][row][col])
+// for every valid grouped row (padding rows are left untouched).
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restrict__ part, int ksplit, long rows,
+                                                            int cols, const int32_t* __restrict__ masked_m,
+                                                            const int32_t* __restrict__ offsets, int nslots,
+                                                            int masked, int M_max, __nv_bfloat16* __restrict__ out) {
+  const long row = blockIdx.x;
+  if (masked) {
+    const int s = (int)(row / M_max);
+    if ((int)(row - (long)s * M_max) >= min(__ldg(masked_m + s), M_max)) return;
+  } else if (row >= __ldg(offsets + nslots)) {
+    return;
+  }
+  for (int c = threadIdx.x * 4; c < cols; c += blockDim.x * 4) {
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int q = 0; q < ksplit; ++q) {
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)q * rows + row) * cols + c));
+      acc.x += v.x;
+      acc.y += v.y;
+      acc.z += v.z;
+      acc.w += v.w;
+    }
+    uint2 o;
+    o.x = pack_bf16x2(acc.x, acc.y);
+    o.y = pack_bf16x2(acc.z, acc.w);
+    *reinterpret_cast<uint2*>(out + (size_t)row * cols + c) = o;
+  }
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -678,7 +694,7 @@ struct Plan {
   bool tm;
   size_t smem;
   uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
-  size_t part_bytes, counter_bytes;
+  size_t part_bytes;
 };
 
 Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
@@ -724,6 +740,12 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   }
   pl.kb_per_split = (pl.kb_total + pl.ksplit - 1) / pl.ksplit;
   pl.ksplit = (pl.kb_total + pl.kb_per_split - 1) / pl.kb_per_split;
+  // the partial sums live in a dense [split][row][column] fp32 workspace; keep it modest
+  const size_t out_cols = (mode == MODE_SWIGLU) ? p.I : p.H;
+  if (pl.ksplit > 1 && (size_t)pl.ksplit * grouped_rows(p) * out_cols * 4 > (size_t(1) << 30)) {
+    pl.ksplit = 1;
+    pl.kb_per_split = pl.kb_total;
+  }
   // shared memory carve (offsets relative to the 1024-aligned base)
   size_t extra = 0;
   auto carve = [&](size_t bytes, size_t align) {
@@ -752,8 +774,7 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
       break;
     }
   }
-  pl.part_bytes = pl.ksplit > 1 ? (size_t)tiles * pl.ksplit * 2 * BN * BM * 4 : 0;
-  pl.counter_bytes = pl.ksplit > 1 ? (size_t)tiles * 4 : 0;
+  pl.part_bytes = pl.ksplit > 1 ? (size_t)pl.ksplit * grouped_rows(p) * out_cols * 4 : 0;
   return pl;
 }
 
@@ -816,14 +837,17 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   prm.pre_off = pl.pre_off;
   prm.bar_off = pl.bar_off;
   prm.misc_off = pl.misc_off;
-  if (pl.ksplit > 1) {
-    char* base = static_cast<char*>(ws);
-    prm.counters = reinterpret_cast<int32_t*>(base);
-    prm.part = reinterpret_cast<float*>(base + align_up(pl.counter_bytes, 256));
-    if (cudaMemsetAsync(prm.counters, 0, pl.counter_bytes, st) != cudaSuccess) return MOE_ERR_CUDA;
-  }
+  prm.rows_total = (long)rowsB;
+  if (pl.ksplit > 1) prm.part = static_cast<float*>(ws);
   kern<<<di.sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], prm);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  if (pl.ksplit > 1) {
+    splitk_reduce_kernel<<<(unsigned)rowsB, 256, 0, st>>>(prm.part, pl.ksplit, (long)rowsB, prm.out_cols, masked_m,
+                                                          offsets, pl.nslots, prm.masked, p.M_max,
+                                                          static_cast<__nv_bfloat16*>(out));
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  return MOE_OK;
 }
 
 // ---------------------------------------------------------------------------
@@ -890,7 +914,7 @@ size_t gemm_workspace_bytes(const moe_problem& p) {
   for (int mode = 0; mode < 2; ++mode) {
     for (int sms : {132, 148, 152, 160, 170, 188, 256}) {
       const Plan pl = make_plan(p, mode, sms, 232448);
-      best = std::max(best, align_up(pl.counter_bytes, 256) + pl.part_bytes);
+      best = std::max(best, pl.part_bytes);
     }
   }
   return best;
