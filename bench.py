@@ -34,7 +34,10 @@ HEADLINE = "mixtral_decode"
 METRIC = "MoE layer tokens/s"
 # ncu DRAM bytes (read + write) per launch of the dominant kernel, keyed by the
 # workload and the hash of the kernel source they were captured from.
-TRAFFIC = {}
+TRAFFIC = {
+    # gate/up kernel, ncu --set full (profiles/gemm_gateup_mixtral_decode.md): 1.880222 GB read + 4.031 MB written
+    "mixtral_decode:dc05c80eeaa0608b": 1884253710,
+}
 
 
 def load_peaks():
@@ -224,11 +227,16 @@ def run_gpu(args, cfg, rank, world, local_rank):
              lambda: L.down(stream), lambda: L.combine(stream)]
     graphs = []
     for fn in parts:
-        g = torch.cuda.CUDAGraph()
+        try:  # keep the graph itself (not only its executable) so its kernel nodes can be counted
+            g = torch.cuda.CUDAGraph(keep_graph=True)
+        except TypeError:
+            g = torch.cuda.CUDAGraph()
         with torch.cuda.graph(g, stream=stream):
             fn()
+        if hasattr(g, "instantiate"):
+            g.instantiate()
         graphs.append(g)
-    n_launch = count_launches(cfg, p2l is not None)
+    n_launch, launch_src = count_launches(graphs, cfg, p2l is not None)
 
     def step():
         for g in graphs:
@@ -293,15 +301,32 @@ def run_gpu(args, cfg, rank, world, local_rank):
     mm = L.masked_m.cpu().numpy()
     touched = int((mm > 0).sum())
     return dict(total_ms=total_ms, part_ms=part_ms, e2e_ms=e2e_ms, masked_m=mm, touched=touched, clocks=clk.summary(),
-                n_launch=n_launch, h2d=xh.numel() * xh.element_size() + lh.numel() * lh.element_size(),
+                n_launch=n_launch, launch_src=launch_src, h2d=xh.numel() * xh.element_size() + lh.numel() * lh.element_size(),
                 d2h=oh.numel() * oh.element_size(), x=x, logits=logits)
 
 
-def count_launches(cfg, with_map):
-    """Kernels (and memsets) one step enqueues: route 1; permute memset + [map] + mark + scan + scatter;
-    gate/up 1; down 1 (+ memset of the split-K counters when it splits); combine 1."""
-    n = 1 + 4 + (1 if with_map else 0) + 1 + 1 + 1
-    return n
+def count_launches(graphs, cfg, with_map):
+    """Kernels of this library in one step: the kernel nodes of the captured graphs
+    (memset nodes excluded).  Falls back to the static count of the calls' kernels
+    (route 1; permute [map] + mark + scan + scatter; gate/up 1; down 1 or 2; combine 1)."""
+    try:
+        import ctypes
+        rt = ctypes.CDLL("libcudart.so.13")
+        total = 0
+        for g in graphs:
+            h = ctypes.c_void_p(g.raw_cuda_graph())
+            n = ctypes.c_size_t(0)
+            if rt.cudaGraphGetNodes(h, None, ctypes.byref(n)) != 0:
+                raise RuntimeError("cudaGraphGetNodes")
+            nodes = (ctypes.c_void_p * n.value)()
+            rt.cudaGraphGetNodes(h, nodes, ctypes.byref(n))
+            for nd in nodes:
+                t = ctypes.c_int(-1)
+                rt.cudaGraphNodeGetType(ctypes.c_void_p(nd), ctypes.byref(t))
+                total += t.value == 0  # cudaGraphNodeTypeKernel
+        return int(total), "graph kernel nodes"
+    except Exception:
+        return 1 + 3 + (1 if with_map else 0) + 1 + 1 + 1, "static count"
 
 
 def gateup_roofline(cfg, res, peaks, moe_src):
@@ -435,6 +460,7 @@ def main():
             "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": res["n_launch"] * K,
+            "gpu_launches_per_step": {"kernels": res["n_launch"], "counted_from": res["launch_src"]},
             "clocks": res["clocks"],
         }
         b13, b2 = expert_bytes(cfg)
