@@ -134,6 +134,22 @@ moe_status moe_check_problem(const moe_problem* p);
  *   (device, written).  One warp per token. */
 moe_status moe_route_topk(const moe_problem* p, const float* logits, int32_t* ids, float* w, moe_stream_t stream);
 
+/* Step 1, DeepSeek-V3 variant ("MoE inference and expert parallelism", routing
+ * section, Table 3-1: sigmoid scoring with e_score_correction_bias, grouped
+ * top-k; the bias decides which experts are chosen, the weights use the
+ * unbiased scores).  Per token: s_e = sigmoid(l_e), key_e = s_e + bias_e;
+ * the E experts form n_group contiguous groups of E/n_group, a group scored by
+ * its largest key; the topk_group best groups are kept, then the K largest
+ * keys among their experts (all ties to the lower index; keys compared in
+ * fp64).  w[t,k] = s_{e_k} (divided by the sum over the K when renormalize),
+ * times scale.
+ *   logits [T][E] fp32, bias [E] fp32 or NULL (device, read); ids [T][K] int32,
+ *   w [T][K] fp32 (device, written).  Requires 1 <= n_group <= 32, E % n_group
+ *   == 0, 1 <= topk_group <= n_group, K <= topk_group * E / n_group. */
+moe_status moe_route_grouped_topk(const moe_problem* p, const float* logits, const float* bias, int32_t n_group,
+                                  int32_t topk_group, int32_t renormalize, float scale, int32_t* ids, float* w,
+                                  moe_stream_t stream);
+
 /* Step 2 (dispatch; "Inference INFRA methodology (5)", section "DeepGEMM";
  * "vLLM EPLB", section 1.2; "MoonEP", sections "Why dynamic routing is hard"
  * and "Zero-copy and static buffer").
@@ -216,6 +232,27 @@ moe_status moe_grouped_down_gemm(const moe_problem* p, const void* hg, const flo
  * [T][K+S], w [T][K] fp32, out [T][H] (p->out). */
 moe_status moe_combine(const moe_problem* p, const void* yg, const int32_t* row_of, const float* w, void* out,
                        moe_stream_t stream);
+
+/* EPLB load statistics ("vLLM EPLB", section 1.2: expert_load_pass and
+ * expert_load_window).  Copies this pass's per-slot row counts masked_m[0..P)
+ * (as written by moe_permute; the shared slot is not recorded) into row
+ * (pass mod window) of load_window [window][P] int32 (device). */
+moe_status moe_eplb_record(const moe_problem* p, const int32_t* masked_m, int64_t pass, int32_t window,
+                           int32_t* load_window, moe_stream_t stream);
+
+/* Rebalance from a load window ("vLLM EPLB", section 1.2: the window's physical
+ * loads are summed per logical expert through physical_to_logical_map, then
+ * replicas are re-assigned).  logical_load [E] int64 = sum over the window and
+ * over the slots holding each expert; new_phys_to_log [P]: slots 0..E-1 hold
+ * experts 0..E-1, slots E..P-1 hold the P-E experts with the largest load in
+ * descending order (ties to the lower index) -- the single-GPU policy of this
+ * library (the page's node / GPU packing is a multi-node control plane).
+ * phys_to_log [P] is the map the window was recorded with (NULL when P == E).
+ * Requires P - E <= E.  A map entry outside [0,E) sets MOE_FLAG_BAD_MAP.  One
+ * CTA; all pointers device. */
+moe_status moe_eplb_rebalance(const moe_problem* p, const int32_t* load_window, int32_t window,
+                              const int32_t* phys_to_log, int64_t* logical_load, int32_t* new_phys_to_log,
+                              int32_t* err_flag, moe_stream_t stream);
 
 /* Host helper ("vLLM EPLB", section 1.2): invert a physical_to_logical map.
  * All pointers are HOST pointers.  p2l [P] in, l2p [E][R] out (slots of each

@@ -56,6 +56,9 @@ def _load():
     lib.orc_e4m3_encode_array.argtypes = [i64, vp, vp]
     lib.orc_bf16_encode_array.argtypes = [i64, vp, vp]
     lib.orc_route.argtypes = [i32, i32, i32, vp, vp, vp]
+    lib.orc_route_grouped.argtypes = [i32, i32, i32, vp, vp, i32, i32, i32, dbl, vp, vp]
+    lib.orc_eplb_rebalance.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+    lib.orc_eplb_rebalance.restype = i32
     lib.orc_eplb_invert.argtypes = [i32, i32, vp, i32, vp, vp]
     lib.orc_eplb_invert.restype = i32
     lib.orc_layout.argtypes = [i32] * 7 + [vp] * 7
@@ -158,6 +161,21 @@ def route(logits, K: int):
     return ids, w
 
 
+def route_grouped(logits, K: int, n_group: int, topk_group: int, bias=None, renormalize: bool = True,
+                  scale: float = 1.0):
+    """Sigmoid scores, bias-corrected grouped top-K: ids [T,K] int32, fp64 weights [T,K]."""
+    logits = _c(logits, np.float32)
+    T, E = logits.shape
+    if E % n_group or not (1 <= topk_group <= n_group) or K > (E // n_group) * topk_group:
+        raise ValueError("inconsistent grouped routing")
+    b = None if bias is None else _c(bias, np.float32)
+    ids = np.empty((T, K), np.int32)
+    w = np.empty((T, K), np.float64)
+    _load().orc_route_grouped(T, E, K, logits.ctypes.data, None if b is None else b.ctypes.data, n_group,
+                              topk_group, int(renormalize), float(scale), ids.ctypes.data, w.ctypes.data)
+    return ids, w
+
+
 def eplb_invert(p2l, E: int, R: int | None = None):
     """physical_to_logical -> (logical_to_physical [E,R], logical_replica_count [E], max replicas)."""
     p2l = _c(p2l, np.int32)
@@ -169,6 +187,22 @@ def eplb_invert(p2l, E: int, R: int | None = None):
     if r < 0:
         raise ValueError("invalid physical_to_logical map (code %d)" % r)
     return l2p[:, :max(r, 1)], rc, r
+
+
+def eplb_rebalance(window, E: int, p2l=None):
+    """Load window [W,P] (+ current map) -> (logical load [E] int64, new physical_to_logical [P])."""
+    win = _c(window, np.int32)
+    W, P = win.shape
+    if P - E > E:
+        raise ValueError("more extra slots than experts")
+    m = None if p2l is None else _c(p2l, np.int32)
+    load = np.empty(E, np.int64)
+    new = np.empty(P, np.int32)
+    r = _load().orc_eplb_rebalance(P, E, W, win.ctypes.data, None if m is None else m.ctypes.data,
+                                   load.ctypes.data, new.ctypes.data)
+    if r < 0:
+        raise ValueError("invalid physical_to_logical map")
+    return load, new
 
 
 def layout(cfg, ids, p2l=None):

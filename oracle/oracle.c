@@ -202,6 +202,67 @@ void orc_route(int T, int E, int K, const float* logits, int32_t* ids, double* w
   }
 }
 
+/* [MoE-EP] routing section, Table 3-1, DeepSeek-V3 row: sigmoid scoring with
+ * e_score_correction_bias, grouped top-k ("first the top groups, then the
+ * experts inside them"); the bias only decides which experts are chosen, the
+ * weights use the unbiased sigmoid score.
+ * Readings: s_e = 1/(1+exp(-l_e)); selection key c_e = s_e + bias_e (bias 0 when
+ * absent); experts form n_group contiguous groups of E/n_group; a group's score
+ * is the largest key in it; the topk_group best groups are kept (ties: lower
+ * group index), then the K best keys among their experts (ties: lower expert
+ * index), listed in that order; w_k = s_{e_k}, divided by their sum when
+ * renormalize, then multiplied by scale.  All in fp64. */
+void orc_route_grouped(int T, int E, int K, const float* logits, const float* bias, int n_group, int topk_group,
+                       int renormalize, double scale, int32_t* ids, double* w) {
+  const int gs = E / n_group;
+#pragma omp parallel
+  {
+    double* sc = (double*)malloc((size_t)E * sizeof(double));
+    double* key = (double*)malloc((size_t)E * sizeof(double));
+    double* gsc = (double*)malloc((size_t)n_group * sizeof(double));
+    char* gsel = (char*)malloc((size_t)n_group);
+    char* taken = (char*)malloc((size_t)E);
+#pragma omp for schedule(static)
+    for (int t = 0; t < T; ++t) {
+      for (int e = 0; e < E; ++e) {
+        sc[e] = 1.0 / (1.0 + exp(-(double)logits[(int64_t)t * E + e]));
+        key[e] = sc[e] + (bias ? (double)bias[e] : 0.0);
+        taken[e] = 0;
+      }
+      for (int g = 0; g < n_group; ++g) {
+        gsc[g] = -INFINITY;
+        for (int e = g * gs; e < (g + 1) * gs; ++e)
+          if (key[e] > gsc[g]) gsc[g] = key[e];
+        gsel[g] = 0;
+      }
+      for (int r = 0; r < topk_group; ++r) {
+        int best = -1;
+        for (int g = 0; g < n_group; ++g)
+          if (!gsel[g] && (best < 0 || gsc[g] > gsc[best])) best = g;
+        gsel[best] = 1;
+      }
+      double sum = 0.0;
+      for (int k = 0; k < K; ++k) {
+        int best = -1;
+        for (int e = 0; e < E; ++e)
+          if (gsel[e / gs] && !taken[e] && (best < 0 || key[e] > key[best])) best = e;
+        taken[best] = 1;
+        ids[(int64_t)t * K + k] = best;
+        sum += sc[best];
+      }
+      for (int k = 0; k < K; ++k) {
+        const double v = sc[ids[(int64_t)t * K + k]];
+        w[(int64_t)t * K + k] = (renormalize ? v / sum : v) * scale;
+      }
+    }
+    free(sc);
+    free(key);
+    free(gsc);
+    free(gsel);
+    free(taken);
+  }
+}
+
 /* ------------------------------------------------------------------------ */
 /* EPLB maps                                                                 */
 /* ------------------------------------------------------------------------ */
@@ -227,6 +288,39 @@ int orc_eplb_invert(int P, int E, const int32_t* p2l, int R, int32_t* l2p, int32
     if (rc[e] > maxr) maxr = rc[e];
   }
   return maxr;
+}
+
+/* [EPLB] section 1.2: expert_load_pass holds each physical slot's token count
+ * for one forward pass (the per-slot row counts, masked_m); the passes of a
+ * window are kept in expert_load_window [W][P]; at a rebalance the window's
+ * physical loads are summed per logical expert through physical_to_logical_map
+ * and replicas are re-assigned.
+ * Reading of the policy (the page's hierarchical / global packing is a
+ * multi-node control plane): slots 0..E-1 keep experts 0..E-1 and the P-E
+ * extra slots hold the P-E experts with the largest load, in descending load
+ * (ties: lower expert index).  window may be NULL for W = 0.  Returns -1 for a
+ * map entry outside [0,E) or sizes with E < 1, P < E or P - E > E, 0
+ * otherwise. */
+int orc_eplb_rebalance(int P, int E, int W, const int32_t* window, const int32_t* p2l, int64_t* logical_load,
+                       int32_t* new_p2l) {
+  if (E <= 0 || P < E || P - E > E) return -1;
+  for (int e = 0; e < E; ++e) logical_load[e] = 0;
+  for (int s = 0; s < P; ++s) {
+    const int e = p2l ? p2l[s] : s;
+    if (e < 0 || e >= E) return -1;
+    for (int w = 0; w < W; ++w) logical_load[e] += window[(int64_t)w * P + s];
+  }
+  for (int e = 0; e < E; ++e) new_p2l[e] = e;
+  char* used = (char*)calloc((size_t)E, 1);
+  for (int r = 0; r < P - E; ++r) {
+    int best = -1;
+    for (int e = 0; e < E; ++e)
+      if (!used[e] && (best < 0 || logical_load[e] > logical_load[best])) best = e;
+    used[best] = 1;
+    new_p2l[E + r] = best;
+  }
+  free(used);
+  return 0;
 }
 
 /* ------------------------------------------------------------------------ */

@@ -23,8 +23,8 @@ LAYOUTS = {"masked": MOE_LAYOUT_MASKED, "contig": MOE_LAYOUT_CONTIG}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_version", "moe_status_string", "moe_grouped_rows", "moe_workspace_bytes", "moe_check_problem",
-           "moe_route_topk", "moe_permute", "moe_permute_no_workspace", "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_combine",
-           "moe_eplb_invert"]
+           "moe_route_topk", "moe_route_grouped_topk", "moe_permute", "moe_permute_no_workspace", "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_combine",
+           "moe_eplb_record", "moe_eplb_rebalance", "moe_eplb_invert"]
 
 
 class MoeError(RuntimeError):
@@ -72,6 +72,8 @@ def lib():
     L.moe_check_problem.restype = i32
     L.moe_route_topk.argtypes = [pp, vp, vp, vp, vp]
     L.moe_route_topk.restype = i32
+    L.moe_route_grouped_topk.argtypes = [pp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
+    L.moe_route_grouped_topk.restype = i32
     L.moe_permute.argtypes = [pp] + [vp] * 11 + [sz, vp]
     L.moe_permute.restype = i32
     L.moe_permute_no_workspace.argtypes = [pp] + [vp] * 11
@@ -82,6 +84,10 @@ def lib():
     L.moe_grouped_down_gemm.restype = i32
     L.moe_combine.argtypes = [pp, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
+    L.moe_eplb_record.argtypes = [pp, vp, i64, i32, vp, vp]
+    L.moe_eplb_record.restype = i32
+    L.moe_eplb_rebalance.argtypes = [pp, vp, i32, vp, vp, vp, vp, vp]
+    L.moe_eplb_rebalance.restype = i32
     L.moe_eplb_invert.argtypes = [i32, i32, vp, i32, vp, vp]
     L.moe_eplb_invert.restype = i32
     _lib = L
@@ -134,6 +140,13 @@ def moe_route_topk(p: Problem, logits, ids, w, stream=None) -> None:
            "moe_route_topk")
 
 
+def moe_route_grouped_topk(p: Problem, logits, bias, n_group: int, topk_group: int, ids, w, renormalize=True,
+                           scale: float = 1.0, stream=None) -> None:
+    _check(lib().moe_route_grouped_topk(ctypes.byref(p), _ptr(logits), _ptr(bias), n_group, topk_group,
+                                        int(bool(renormalize)), float(scale), _ptr(ids), _ptr(w), _stream(stream)),
+           "moe_route_grouped_topk")
+
+
 def moe_permute(p: Problem, ids, x, phys_to_log, masked_m, offsets, row_of, src_of, xg, xg_scales, err_flag,
                 workspace, stream=None) -> None:
     nbytes = workspace.numel() * workspace.element_size()
@@ -170,6 +183,18 @@ def moe_grouped_down_gemm(p: Problem, hg, hg_scales, w2, w2_scales, masked_m, of
 def moe_combine(p: Problem, yg, row_of, w, out, stream=None) -> None:
     _check(lib().moe_combine(ctypes.byref(p), _ptr(yg), _ptr(row_of), _ptr(w), _ptr(out), _stream(stream)),
            "moe_combine")
+
+
+def moe_eplb_record(p: Problem, masked_m, pass_index: int, window: int, load_window, stream=None) -> None:
+    _check(lib().moe_eplb_record(ctypes.byref(p), _ptr(masked_m), int(pass_index), int(window), _ptr(load_window),
+                                 _stream(stream)), "moe_eplb_record")
+
+
+def moe_eplb_rebalance(p: Problem, load_window, window: int, phys_to_log, logical_load, new_phys_to_log, err_flag,
+                       stream=None) -> None:
+    _check(lib().moe_eplb_rebalance(ctypes.byref(p), _ptr(load_window), int(window), _ptr(phys_to_log),
+                                    _ptr(logical_load), _ptr(new_phys_to_log), _ptr(err_flag), _stream(stream)),
+           "moe_eplb_rebalance")
 
 
 def moe_eplb_invert(p2l, E: int, R: int):

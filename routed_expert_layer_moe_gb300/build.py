@@ -15,7 +15,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmoe_gb300.so")
-SOURCES = ["api.cu", "route.cu", "permute.cu", "permute_static.cu", "gemm_tc.cu", "combine.cu"]
+SOURCES = ["api.cu", "route.cu", "permute.cu", "permute_static.cu", "gemm_tc.cu", "combine.cu", "eplb.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -161,6 +161,19 @@ moe_status moe_route_topk(const moe_problem* p, const float* logits, int32_t* id
   return launched(launch_route(*p, logits, ids, w, (cudaStream_t)stream));
 }
 
+moe_status moe_route_grouped_topk(const moe_problem* p, const float* logits, const float* bias, int32_t n_group,
+                                  int32_t topk_group, int32_t renormalize, float scale, int32_t* ids, float* w,
+                                  moe_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return (moe_status)r;
+  if (n_group < 1 || n_group > 32 || p->E % n_group || topk_group < 1 || topk_group > n_group ||
+      p->K > topk_group * (p->E / n_group))
+    return MOE_ERR_INVALID;
+  if (p->T > 0 && (!logits || !ids || !w)) return MOE_ERR_INVALID;
+  return launched(launch_route_grouped(*p, logits, bias, n_group, topk_group, renormalize != 0, scale, ids, w,
+                                       (cudaStream_t)stream));
+}
+
 moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, const int32_t* phys_to_log,
                        int32_t* masked_m, int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg,
                        float* xg_scales, int32_t* err_flag, void* workspace, size_t workspace_bytes,
@@ -215,6 +228,26 @@ moe_status moe_combine(const moe_problem* p, const void* yg, const int32_t* row_
   if (p->T > 0 && (!yg || !row_of || !w || !out)) return MOE_ERR_INVALID;
   if (p->T > 0 && (!aligned16(yg) || !aligned16(out))) return MOE_ERR_UNSUPPORTED;
   return launched(launch_combine(*p, yg, row_of, w, out, (cudaStream_t)stream));
+}
+
+moe_status moe_eplb_record(const moe_problem* p, const int32_t* masked_m, int64_t pass, int32_t window,
+                           int32_t* load_window, moe_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return (moe_status)r;
+  if (!masked_m || !load_window || window < 1 || pass < 0) return MOE_ERR_INVALID;
+  return launched(launch_eplb_record(*p, masked_m, pass, window, load_window, (cudaStream_t)stream));
+}
+
+moe_status moe_eplb_rebalance(const moe_problem* p, const int32_t* load_window, int32_t window,
+                              const int32_t* phys_to_log, int64_t* logical_load, int32_t* new_phys_to_log,
+                              int32_t* err_flag, moe_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return (moe_status)r;
+  if (!load_window || window < 1 || !logical_load || !new_phys_to_log || !err_flag) return MOE_ERR_INVALID;
+  if (!phys_to_log && p->P != p->E) return MOE_ERR_INVALID;
+  if (p->P - p->E > p->E) return MOE_ERR_INVALID;  // each extra slot holds a different expert
+  return launched(launch_eplb_rebalance(*p, load_window, window, phys_to_log, logical_load, new_phys_to_log,
+                                        err_flag, (cudaStream_t)stream));
 }
 
 int32_t moe_eplb_invert(int32_t P, int32_t E, const int32_t* p2l, int32_t R, int32_t* l2p, int32_t* rc) {

@@ -29,6 +29,8 @@ CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t
 
 // Per-call launchers (each returns a moe_status).
 int launch_route(const moe_problem& p, const float* logits, int32_t* ids, float* w, cudaStream_t st);
+int launch_route_grouped(const moe_problem& p, const float* logits, const float* bias, int n_group, int topk_group,
+                         int renorm, float scale, int32_t* ids, float* w, cudaStream_t st);
 int launch_permute(const moe_problem& p, const int32_t* ids, const void* x, const int32_t* p2l, int32_t* masked_m,
                    int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg, float* xg_scales, int32_t* err,
                    void* ws, cudaStream_t st);
@@ -37,6 +39,10 @@ int launch_gemm(const moe_problem& p, int mode, const void* a_act, const float* 
                 const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out,
                 float* out_scales, int32_t* err, void* ws, cudaStream_t st);
 size_t gemm_workspace_bytes(const moe_problem& p);
+int launch_eplb_record(const moe_problem& p, const int32_t* masked_m, int64_t pass, int window, int32_t* load_window,
+                       cudaStream_t st);
+int launch_eplb_rebalance(const moe_problem& p, const int32_t* load_window, int window, const int32_t* p2l,
+                          int64_t* logical_load, int32_t* new_p2l, int32_t* err, cudaStream_t st);
 int launch_combine(const moe_problem& p, const void* yg, const int32_t* row_of, const float* w, void* out,
                    cudaStream_t st);
 

@@ -423,7 +423,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<F8>::epi));
     // ------------------------------------------------------------ epilogue
-    const int etid = tid - EPI_WARP0 * 32;
     const int quarter = warp & 3;             // tensor-memory lane quarter this warp may access
     const int half = (warp - EPI_WARP0) >> 2; // column half (warpgroup 1 or 2)
     const int lrow = quarter * 32 + lane;     // tensor-memory lane of this thread

@@ -72,6 +72,117 @@ void launch_route_per(const moe_problem& p, const float* logits, int32_t* ids, f
   route_topk_kernel<PER><<<blocks, threads, 0, st>>>(logits, p.T, p.E, p.K, ids, w);
 }
 
+// "MoE inference and expert parallelism", routing section, Table 3-1 (DeepSeek-V3):
+// sigmoid scores, e_score_correction_bias used for the choice only, grouped
+// top-k (the best topk_group of n_group contiguous expert groups, a group
+// scored by its best biased score, then the K best experts inside them).  The
+// keys are compared in fp64 (ties to the lower index); weights are the unbiased
+// scores of the chosen experts, renormalised if asked, times `scale`.
+template <int PER>
+__global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restrict__ logits,
+                                                            const float* __restrict__ bias, int T, int E, int K,
+                                                            int n_group, int topk_group, int renorm, float scale,
+                                                            int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  if (t >= T) return;
+  const float* l = logits + (size_t)t * E;
+  const int gs = E / n_group;
+  double sc[PER], key[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    sc[i] = 0.0;
+    key[i] = -INFINITY;
+    if (e < E) {
+      sc[i] = 1.0 / (1.0 + exp(-(double)__ldg(l + e)));
+      key[i] = sc[i] + (bias ? (double)__ldg(bias + e) : 0.0);
+    }
+  }
+  // group maxima: lane g keeps the score of group g
+  double gmine = -INFINITY;
+  for (int g = 0; g < n_group; ++g) {
+    double m = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (e < E && e / gs == g) m = fmax(m, key[i]);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, off));
+    if (lane == g) gmine = m;
+  }
+  // the topk_group best groups (ties to the lower group index)
+  uint32_t gsel = 0;
+  for (int r = 0; r < topk_group; ++r) {
+    double bv = (lane < n_group && !((gsel >> lane) & 1u)) ? gmine : -INFINITY;
+    int bg = (lane < n_group && !((gsel >> lane) & 1u)) ? lane : 0x7fffffff;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const int og = __shfl_xor_sync(0xffffffffu, bg, off);
+      if (og != 0x7fffffff && (bg == 0x7fffffff || ov > bv || (ov == bv && og < bg))) {
+        bv = ov;
+        bg = og;
+      }
+    }
+    gsel |= 1u << bg;
+  }
+  uint32_t avail = 0;
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    if (e < E && ((gsel >> (e / gs)) & 1u)) avail |= 1u << i;
+  }
+  int my_id = 0;
+  double my_sc = 0.0;
+  for (int k = 0; k < K; ++k) {
+    double bv = -INFINITY, bs = 0.0;
+    int be = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      if ((avail >> i) & 1u) {
+        if (be == 0x7fffffff || key[i] > bv) {
+          bv = key[i];
+          bs = sc[i];
+          be = lane + 32 * i;
+        }
+      }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const double os = __shfl_xor_sync(0xffffffffu, bs, off);
+      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+      if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
+        bv = ov;
+        bs = os;
+        be = oe;
+      }
+    }
+    if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
+    if (lane == k) {
+      my_id = be;
+      my_sc = bs;
+    }
+  }
+  double sum = 0.0;
+  for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, my_sc, k);  // fixed order
+  if (lane < K) {
+    ids[(size_t)t * K + lane] = my_id;
+    w[(size_t)t * K + lane] = (float)((renorm ? my_sc / sum : my_sc) * (double)scale);
+  }
+}
+
+template <int PER>
+void launch_grouped_per(const moe_problem& p, const float* logits, const float* bias, int n_group, int topk_group,
+                        int renorm, float scale, int32_t* ids, float* w, cudaStream_t st) {
+  const int threads = 256;
+  const int blocks = (int)(((int64_t)p.T * 32 + threads - 1) / threads);
+  route_grouped_kernel<PER><<<blocks, threads, 0, st>>>(logits, bias, p.T, p.E, p.K, n_group, topk_group, renorm,
+                                                        scale, ids, w);
+}
+
 }  // namespace
 
 int launch_route(const moe_problem& p, const float* logits, int32_t* ids, float* w, cudaStream_t st) {
@@ -89,6 +200,25 @@ int launch_route(const moe_problem& p, const float* logits, int32_t* ids, float*
     launch_route_per<16>(p, logits, ids, w, st);
   else
     launch_route_per<32>(p, logits, ids, w, st);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_route_grouped(const moe_problem& p, const float* logits, const float* bias, int n_group, int topk_group,
+                         int renorm, float scale, int32_t* ids, float* w, cudaStream_t st) {
+  if (p.T == 0) return MOE_OK;
+  const int per = (p.E + 31) / 32;
+  if (per <= 1)
+    launch_grouped_per<1>(p, logits, bias, n_group, topk_group, renorm, scale, ids, w, st);
+  else if (per <= 2)
+    launch_grouped_per<2>(p, logits, bias, n_group, topk_group, renorm, scale, ids, w, st);
+  else if (per <= 4)
+    launch_grouped_per<4>(p, logits, bias, n_group, topk_group, renorm, scale, ids, w, st);
+  else if (per <= 8)
+    launch_grouped_per<8>(p, logits, bias, n_group, topk_group, renorm, scale, ids, w, st);
+  else if (per <= 16)
+    launch_grouped_per<16>(p, logits, bias, n_group, topk_group, renorm, scale, ids, w, st);
+  else
+    launch_grouped_per<32>(p, logits, bias, n_group, topk_group, renorm, scale, ids, w, st);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -284,3 +284,101 @@ def test_rerun_bitwise_identical(workloads, name):
     for _ in range(2):
         b = to_host(L.forward(x, lg).clone())
         assert (a == b).all()
+
+
+# ---- DeepSeek-V3 routing: sigmoid scores, correction bias, grouped top-k ------------
+
+@pytest.mark.parametrize("T,E,K,ng,tg,with_bias", [(128, 256, 8, 8, 4, True), (37, 64, 6, 8, 3, False),
+                                                    (5, 32, 4, 1, 1, False), (64, 512, 10, 16, 4, True),
+                                                    (9, 8, 2, 4, 2, True)])
+def test_route_grouped(T, E, K, ng, tg, with_bias):
+    logits = mi.normal(4, 88, (T, E), dtype="f32")
+    logits[0, :] = 0.25                       # all keys tie
+    if T > 3:
+        logits[3, ::2] = logits[3, 1]         # many ties
+    bias = (0.05 * mi.normal(4, 89, (E,), dtype="f32")).astype(np.float32) if with_bias else None
+    ids, w = oracle.route_grouped(logits, K, ng, tg, bias=bias, renormalize=True, scale=2.5)
+    p = moe.Problem.make(T=T, H=128, I=128, E=E, K=K, M_max=T, act="bf16", wt="bf16", out="bf16")
+    gids = torch.empty((T, K), dtype=torch.int32, device="cuda")
+    gw = torch.empty((T, K), dtype=torch.float32, device="cuda")
+    moe.moe_route_grouped_topk(p, to_dev(logits), to_dev(bias), ng, tg, gids, gw, renormalize=True, scale=2.5)
+    torch.cuda.synchronize()
+    assert (to_host(gids) == ids).all()
+    np.testing.assert_allclose(to_host(gw), w, rtol=2e-6, atol=1e-7)
+
+
+def test_route_grouped_rejects_bad_groups():
+    p = moe.Problem.make(T=4, H=128, I=128, E=12, K=4, M_max=4, act="bf16", wt="bf16", out="bf16")
+    t = torch.empty(64, dtype=torch.float32, device="cuda")
+    for ng, tg in ((5, 2), (4, 0), (4, 5), (12, 1)):  # 12 % 5, no group, too many groups, K > 1 * 1
+        with pytest.raises(moe.MoeError):
+            moe.moe_route_grouped_topk(p, t, None, ng, tg, t, t)
+
+
+# ---- f EPLB load statistics -------------------------------------------------------
+
+@pytest.mark.parametrize("name", ["e4m3_eplb_zipf", "bf16_masked"])
+def test_eplb_record_and_rebalance(workloads, name):
+    """Record masked_m of several dispatch passes into a wrapping window, then rebalance."""
+    wl = workloads[name]
+    cfg = wl.cfg
+    W, passes = 3, 5
+    win = torch.full((W, cfg.P), SENT_I32, dtype=torch.int32, device="cuda")
+    want = np.full((W, cfg.P), SENT_I32, np.int32)
+    for ps in range(passes):
+        logits = mi.normal(8, 300 + ps, (cfg.T, cfg.E), dtype="f32")
+        ids, _ = oracle.route(logits, cfg.K)
+        Lp = run_permute(wl, ids)
+        moe.moe_eplb_record(Lp.p, Lp.masked_m, ps, W, win)
+        want[ps % W] = oracle.layout(cfg, ids, wl.p2l)["masked_m"][:cfg.P]
+    torch.cuda.synchronize()
+    assert (to_host(win) == want).all()
+    load, new = oracle.eplb_rebalance(want, cfg.E, wl.p2l)
+    gl = torch.empty(cfg.E, dtype=torch.int64, device="cuda")
+    gn = torch.full((cfg.P,), SENT_I32, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    p2l = None if wl.p2l is None else torch.from_numpy(wl.p2l).cuda()
+    moe.moe_eplb_rebalance(wl.problem, win, W, p2l, gl, gn, err)
+    torch.cuda.synchronize()
+    assert int(to_host(err)[0]) == 0
+    assert (to_host(gl) == load).all()
+    assert (to_host(gn) == new).all()
+
+
+@pytest.mark.parametrize("E,P,W", [(8, 16, 4), (256, 288, 10), (1024, 1024, 2), (64, 96, 1)])
+def test_eplb_rebalance_ties_and_sizes(E, P, W):
+    rng = np.random.default_rng(E + P)
+    window = rng.integers(0, 4, size=(W, P)).astype(np.int32)   # small counts: many equal loads
+    p2l = None if P == E else mi.replica_map(rng.integers(0, 50, size=E), E, P - E)
+    load, new = oracle.eplb_rebalance(window, E, p2l)
+    p = moe.Problem.make(T=1, H=128, I=128, E=E, K=1, P=P, M_max=1)
+    gl = torch.empty(E, dtype=torch.int64, device="cuda")
+    gn = torch.empty(P, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_eplb_rebalance(p, to_dev(window), W, None if p2l is None else to_dev(p2l), gl, gn, err)
+    torch.cuda.synchronize()
+    assert int(to_host(err)[0]) == 0
+    assert (to_host(gl) == load).all()
+    assert (to_host(gn) == new).all()
+
+
+def test_eplb_rebalance_flags_and_rejects():
+    E, P, W = 8, 12, 2
+    p = moe.Problem.make(T=1, H=128, I=128, E=E, K=1, P=P, M_max=1)
+    window = torch.ones((W, P), dtype=torch.int32, device="cuda")
+    gl = torch.empty(E, dtype=torch.int64, device="cuda")
+    gn = torch.empty(P, dtype=torch.int32, device="cuda")
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    bad = torch.tensor([0, 1, 2, 3, 4, 5, 6, 7, 0, 8, 1, -1], dtype=torch.int32, device="cuda")
+    moe.moe_eplb_rebalance(p, window, W, bad, gl, gn, err)
+    torch.cuda.synchronize()
+    assert int(to_host(err)[0]) & moe.MOE_FLAG_BAD_MAP
+    with pytest.raises(moe.MoeError):      # no map although P != E
+        moe.moe_eplb_rebalance(p, window, W, None, gl, gn, err)
+    with pytest.raises(moe.MoeError):      # empty window
+        moe.moe_eplb_rebalance(p, window, 0, bad, gl, gn, err)
+    p2 = moe.Problem.make(T=1, H=128, I=128, E=4, K=1, P=12, M_max=1)
+    with pytest.raises(moe.MoeError):      # more extra slots than experts
+        moe.moe_eplb_rebalance(p2, window, W, bad, gl, gn, err)
+    with pytest.raises(moe.MoeError):
+        moe.moe_eplb_record(p, window, 0, 0, window)

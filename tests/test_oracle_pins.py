@@ -356,3 +356,88 @@ def test_coverage_formula_monte_carlo():
         touched.append(len(np.unique(ids)))
     C = 1.0 - (1.0 - K / E) ** T
     assert abs(np.mean(touched) - E * C) < 1.5
+
+
+# ---- sigmoid + bias grouped routing ("MoE inference and expert parallelism", Table 3-1) ----
+
+def _sig(x):
+    return scipy.special.expit(np.asarray(x, np.float64))
+
+
+def test_grouped_route_worked_example():
+    """E = 8 in 4 groups of 2, keep 2 groups, K = 2.  Group maxima (logits) are 5, 1, 4, 3,
+    so groups {0,1} and {4,5} survive and experts 6, 7 (logit 3) are excluded although
+    their logits beat expert 0's and 5's."""
+    l = np.array([[0.0, 5.0, 1.0, 1.0, 4.0, 0.0, 3.0, 3.0]], np.float32)
+    ids, w = oracle.route_grouped(l, 2, n_group=4, topk_group=2)
+    assert ids.tolist() == [[1, 4]]
+    s = _sig([5.0, 4.0])
+    np.testing.assert_allclose(w[0], s / s.sum(), rtol=1e-14)
+    # a bias of +1 on expert 7 lifts its group and wins the selection; the weight stays unbiased
+    bias = np.array([0, 0, 0, 0, 0, 0, 0, 1.0], np.float32)
+    ids, w = oracle.route_grouped(l, 2, n_group=4, topk_group=2, bias=bias)
+    assert ids.tolist() == [[7, 1]]
+    s = _sig([3.0, 5.0])
+    np.testing.assert_allclose(w[0], s / s.sum(), rtol=1e-14)
+    # without renormalisation, with a scaling factor
+    ids, w = oracle.route_grouped(l, 2, n_group=4, topk_group=2, renormalize=False, scale=2.5)
+    np.testing.assert_allclose(w[0], 2.5 * _sig([5.0, 4.0]), rtol=1e-14)
+
+
+def test_grouped_route_one_group_is_sorted_topk():
+    """One group and no bias: sigmoid is increasing, so the choice is the stable sort of the logits."""
+    logits = mi.normal(2, 41, (30, 64), dtype="f32")
+    ids, w = oracle.route_grouped(logits, 6, n_group=1, topk_group=1)
+    ref = np.argsort(-logits.astype(np.float64), axis=1, kind="stable")[:, :6]
+    assert (ids == ref).all()
+    s = np.take_along_axis(_sig(logits), ref, 1)
+    np.testing.assert_allclose(w, s / s.sum(1, keepdims=True), rtol=1e-13)
+
+
+def test_grouped_route_brute_force_sorting():
+    """Tiny inputs against the definition written with sorts instead of repeated arg-max."""
+    rng = np.random.default_rng(5)
+    for _ in range(200):
+        ng = int(rng.choice([1, 2, 4]))
+        gs = int(rng.integers(1, 4))
+        E = ng * gs
+        tg = int(rng.integers(1, ng + 1))
+        K = int(rng.integers(1, tg * gs + 1))
+        l = np.round(rng.standard_normal((1, E)) * 2, 1).astype(np.float32)  # rounding creates ties
+        bias = (np.round(rng.standard_normal(E), 1).astype(np.float32) if rng.random() < 0.5 else None)
+        ids, _ = oracle.route_grouped(l, K, ng, tg, bias=bias)
+        key = _sig(l[0]) + (0 if bias is None else bias.astype(np.float64))
+        gmax = [max(key[g * gs:(g + 1) * gs]) for g in range(ng)]
+        groups = sorted(range(ng), key=lambda g: (-gmax[g], g))[:tg]
+        cand = [e for e in range(E) if e // gs in groups]
+        ref = sorted(cand, key=lambda e: (-key[e], e))[:K]
+        assert ids[0].tolist() == ref
+
+
+# ---- EPLB load statistics (vLLM EPLB, section 1.2) ---------------------------------------
+
+def test_eplb_rebalance_worked_map():
+    """The page's map [0,1,2,3,0,1]: slots P0/P4 hold E0 and P1/P5 hold E1, so a
+    window's physical loads fold onto the logical experts through the map."""
+    win = np.array([[10, 4, 3, 2, 6, 1], [5, 1, 7, 0, 2, 0]], np.int32)
+    load, new = oracle.eplb_rebalance(win, 4, p2l=[0, 1, 2, 3, 0, 1])
+    assert load.tolist() == [10 + 6 + 5 + 2, 4 + 1 + 1 + 0, 3 + 7, 2 + 0]
+    assert new.tolist() == [0, 1, 2, 3, 0, 2]  # the two extra slots go to the two hottest
+
+
+def test_eplb_rebalance_counts_match_routing():
+    """Recording masked_m of a pass and folding it through the map gives back the
+    per-expert routing counts (the replica split does not lose or add tokens)."""
+    cfg = SMALL["e4m3_eplb_zipf"]
+    x, logits = mi.activations(cfg)
+    ids, _ = oracle.route(logits, cfg.K)
+    counts = np.bincount(ids.ravel(), minlength=cfg.E)
+    p2l = mi.replica_map(counts, cfg.E, cfg.redundant)
+    lay = oracle.layout(cfg, ids, p2l)
+    win = lay["masked_m"][None, :cfg.P].astype(np.int32)
+    load, new = oracle.eplb_rebalance(win, cfg.E, p2l)
+    assert (load == counts).all()
+    hottest = sorted(range(cfg.E), key=lambda e: (-counts[e], e))[:cfg.redundant]
+    assert new[cfg.E:].tolist() == hottest and new[:cfg.E].tolist() == list(range(cfg.E))
+    # the rebalanced map reproduces the replica rule used to build the workload
+    assert (new == p2l).all()
