@@ -160,7 +160,7 @@ class ClockSampler:
 
 def problem_of(cfg, moe):
     return moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, P=cfg.P, M_max=cfg.M_max,
-                            has_shared=cfg.S, act=cfg.act, wt=cfg.gemm, out=cfg.out, layout=cfg.layout)
+                            has_shared=cfg.S, act=cfg.act, wt=cfg.wt, out=cfg.out, layout=cfg.layout)
 
 
 def to_dev(a, torch, dev):
@@ -171,11 +171,11 @@ def to_dev(a, torch, dev):
 
 
 def expert_bytes(cfg):
-    """Bytes of one expert's weights (W13 + W2, plus fp32 block scales for e4m3)."""
-    esz = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.gemm]
-    b13 = 2 * cfg.I * cfg.H * esz
-    b2 = cfg.H * cfg.I * esz
-    if cfg.gemm == "e4m3":
+    """Bytes of one expert's weights (W13 + W2, plus fp32 block scales for e4m3 / e2m1)."""
+    esz = {"f32": 4, "bf16": 2, "e4m3": 1, "e2m1": 0.5}[cfg.wt]
+    b13 = int(2 * cfg.I * cfg.H * esz)
+    b2 = int(cfg.H * cfg.I * esz)
+    if cfg.wt in ("e4m3", "e2m1"):
         b13 += (2 * cfg.I // 128) * (cfg.H // 128) * 4
         b2 += (cfg.H // 128) * (cfg.I // 128) * 4
     return b13, b2
@@ -198,7 +198,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     p2l = None
     if cfg.redundant:
         pr = moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, M_max=max(cfg.M_max, 1),
-                              act=cfg.act, wt=cfg.gemm, out=cfg.out, layout=cfg.layout)
+                              act=cfg.act, wt=cfg.wt, out=cfg.out, layout=cfg.layout)
         ids = torch.empty((cfg.T, cfg.K), dtype=torch.int32, device=dev)
         wts = torch.empty((cfg.T, cfg.K), dtype=torch.float32, device=dev)
         moe.moe_route_topk(pr, to_dev(logits, torch, dev), ids, wts)
@@ -212,7 +212,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
         t = to_dev(a, torch, dev)
         return t.index_select(0, order).contiguous() if (cfg.redundant or t.shape[0] != order.numel()) else t
 
-    L = moe.MoeLayer(p, cfg.act, cfg.gemm, cfg.out, slots(w13), slots(w2), slots(w13s), slots(w2s),
+    L = moe.MoeLayer(p, cfg.act, cfg.wt, cfg.out, slots(w13), slots(w2), slots(w13s), slots(w2s),
                      phys_to_log=None if p2l is None else torch.from_numpy(p2l).to(dev), device=dev)
     del w13, w2, w13s, w2s
     xd, ld = to_dev(x, torch, dev), to_dev(logits, torch, dev)
@@ -298,11 +298,59 @@ def run_gpu(args, cfg, rank, world, local_rank):
         e2e_ms = float(t.item())
     assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
 
+    aux = aux_timings(moe, L, cfg, ld, stream, torch) if world == 1 else None
     mm = L.masked_m.cpu().numpy()
     touched = int((mm > 0).sum())
     return dict(total_ms=total_ms, part_ms=part_ms, e2e_ms=e2e_ms, masked_m=mm, touched=touched, clocks=clk.summary(),
                 n_launch=n_launch, launch_src=launch_src, h2d=xh.numel() * xh.element_size() + lh.numel() * lh.element_size(),
-                d2h=oh.numel() * oh.element_size(), x=x, logits=logits)
+                d2h=oh.numel() * oh.element_size(), x=x, logits=logits, aux=aux)
+
+
+def grouped_router_params(cfg):
+    """n_group / topk_group for the grouped router on this workload (8 groups, 4 kept, when E allows)."""
+    ng = 8 if cfg.E % 8 == 0 else 1
+    tg = max(1, ng // 2)
+    while tg < ng and cfg.K > tg * (cfg.E // ng):
+        tg += 1
+    return ng, tg
+
+
+def aux_timings(moe, L, cfg, ld, stream, torch, reps=50, window=16):
+    """Device time of the calls outside the layer step: the grouped router on this
+    workload's logits, one EPLB record of masked_m, one EPLB rebalance of a
+    window.  Each is captured `reps` times in one graph; time / reps."""
+    ng, tg = grouped_router_params(cfg)
+    dev = ld.device
+    win = torch.zeros((window, cfg.P), dtype=torch.int32, device=dev)
+    ll = torch.empty(cfg.E, dtype=torch.int64, device=dev)
+    newmap = torch.empty(cfg.P, dtype=torch.int32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+    ids = torch.empty_like(L.ids)
+    w = torch.empty_like(L.w)
+    calls = {
+        "route_grouped": lambda: moe.moe_route_grouped_topk(L.p, ld, None, ng, tg, ids, w, stream=stream),
+        "route_softmax": lambda: moe.moe_route_topk(L.p, ld, ids, w, stream),
+        "eplb_record": lambda i: moe.moe_eplb_record(L.p, L.masked_m, i, window, win, stream),
+        "eplb_rebalance": lambda: moe.moe_eplb_rebalance(L.p, win, window, L.p2l, ll, newmap, err, stream),
+    }
+    out = {"grouped_router": {"n_group": ng, "topk_group": tg}, "eplb_window": window}
+    for name, fn in calls.items():
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            for i in range(reps):
+                fn(i) if name == "eplb_record" else fn()
+        for _ in range(3):
+            g.replay()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            e0.record(stream)
+            for _ in range(4):
+                g.replay()
+            e1.record(stream)
+        stream.synchronize()
+        out[name + "_us"] = round(e0.elapsed_time(e1) * 1e3 / (4 * reps), 2)
+    assert int(err.item()) == 0, "EPLB rebalance flagged %d" % int(err.item())
+    return out
 
 
 def count_launches(graphs, cfg, with_map):
@@ -401,7 +449,7 @@ def run_reference(args, cfg, rank):
 def config_dict(cfg, n):
     return {"workload": cfg.name, "description": cfg.description, "tokens_per_step": cfg.T, "H": cfg.H, "I": cfg.I,
             "E": cfg.E, "K": cfg.K, "shared_experts": cfg.S, "physical_slots": cfg.P, "layout": cfg.layout,
-            "M_max": cfg.M_max, "expert_dtype": cfg.gemm, "parallelism": "replicas%d" % n if n > 1 else "single-gpu",
+            "M_max": cfg.M_max, "expert_dtype": cfg.wt, "parallelism": "replicas%d" % n if n > 1 else "single-gpu",
             "l2": "expert weights exceed L2 (129 MB), no flush" if expert_bytes(cfg)[0] * cfg.E > 2 * 129e6
             else "small workload: L2-resident (launch-latency bound)"}
 
@@ -449,7 +497,8 @@ def main():
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": cfg.gemm, "data": "synthetic (seeded generator, random-init experts)",
+            "vs_baseline": None, "dtype": cfg.gemm if cfg.wt == cfg.gemm else "%s x %s" % (cfg.wt, cfg.gemm),
+            "data": "synthetic (seeded generator, random-init experts)",
             "config": config_dict(cfg, world),
             "roofline": gateup_roofline(cfg, res, peaks, moe_src),
             "step_breakdown_us": {"route+permute": round(res["part_ms"][0] * 1e3, 2),
@@ -457,6 +506,7 @@ def main():
                                   "down": round(res["part_ms"][2] * 1e3, 2),
                                   "combine": round(res["part_ms"][3] * 1e3, 2)},
             "touched_slots": res["touched"],
+            "aux_calls_us": res["aux"],
             "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": res["n_launch"] * K,

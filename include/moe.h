@@ -45,13 +45,20 @@
  *     intermediate, E logical routed experts, K experts per token, P physical
  *     slots (P == E without a replica map), S = has_shared (0/1).  The shared
  *     expert, when present, is slot P.
- *   - Dtypes: bf16 is IEEE binary32's upper half, e4m3 is OCP FP8 E4M3.
+ *   - Dtypes: bf16 is IEEE binary32's upper half, e4m3 is OCP FP8 E4M3,
+ *     e2m1 is OCP FP4 E2M1 (weights only; the FP4 experts of "Inference INFRA
+ *     methodology (5)", shape-evolution table, DS-V4-Pro row).
  *     Supported combinations (act / wt / out): F32/F32/F32, BF16/BF16/BF16,
- *     BF16/E4M3/BF16.  `wt` is the type of the expert weights and of the
- *     grouped activations Xg and Hg.  Yg is F32 when wt is F32, else BF16.
- *   - e4m3 scales are fp32: weights one per 128x128 block
+ *     BF16/E4M3/BF16, BF16/E2M1/BF16.  `wt` is the type of the expert
+ *     weights; the grouped activations Xg and Hg are of type wt, except that
+ *     they are E4M3 when wt is E2M1.  Yg is F32 when wt is F32, else BF16.
+ *   - e4m3 and e2m1 scales are fp32: weights one per 128x128 block
  *     ([slots][N/128][K/128]), grouped activations one per 1x128 group
  *     ([rows][cols/128]).  Quantised value = code * scale.
+ *   - e2m1 weights are packed two codes per byte along the reduced
+ *     dimension: byte j of a row holds column 2j in bits 0-3 and column 2j+1
+ *     in bits 4-7 (a row of K codes is K/2 bytes).  Their base address must
+ *     be 32-byte aligned.
  *   - Weights are stored transposed with the reduced dimension contiguous:
  *     W13 [P+S][2I][H] (rows 0..I-1 = gate W1^T, rows I..2I-1 = up W3^T),
  *     W2 [P+S][H][I].  Slot s holds the weights of the logical expert
@@ -79,7 +86,7 @@ typedef enum moe_status {
   MOE_ERR_WORKSPACE = -4    /* workspace smaller than moe_workspace_bytes() */
 } moe_status;
 
-typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2 } moe_dtype;
+typedef enum moe_dtype { MOE_F32 = 0, MOE_BF16 = 1, MOE_E4M3 = 2, MOE_E2M1 = 3 } moe_dtype;
 
 typedef enum moe_layout { MOE_LAYOUT_MASKED = 0, MOE_LAYOUT_CONTIG = 1 } moe_layout;
 
@@ -165,7 +172,8 @@ moe_status moe_route_grouped_topk(const moe_problem* p, const float* logits, con
  *   row_of [T][K+S] int32: grouped row of record (t,k); column K is the
  *     shared expert's row.  -1 for a record that was not placed (see err_flag).
  *   src_of [rows] int32: token of each written row (padding rows untouched).
- *   xg [rows][H], dtype p->wt: x[t] copied to its rows; for e4m3 each row is
+ *   xg [rows][H], dtype p->wt (e4m3 for E2M1 weights): x[t] copied to its
+ *     rows; for e4m3 each row is
  *     quantised per 1x128 group: s = amax/448 (fp32 IEEE division, s = 1 for an
  *     all-zero group), code = e4m3(x / s) nearest-even, saturating.
  *   xg_scales [rows][H/128] fp32: the group scales (e4m3 only, else NULL).
@@ -207,11 +215,13 @@ moe_status moe_permute_no_workspace(const moe_problem* p, const int32_t* ids, co
  * FP8 accumulated in FP32 once per 128-wide K block).
  * For every slot s and row r < masked_m[s] (row index per the layout):
  *   g = W1[s] . xg[row], u = W3[s] . xg[row], h = SiLU(g) * u
- *   hg[row][0..I) = h, stored as p->wt (e4m3: 1x128 groups as in moe_permute,
- *   scales in hg_scales [rows][I/128]; bf16: nearest-even; f32: as is).
- *   xg_scales / w13_scales / hg_scales: e4m3 only, else NULL.
+ *   hg[row][0..I) = h, stored as p->wt (e4m3 for E2M1 weights; e4m3: 1x128
+ *   groups as in moe_permute, scales in hg_scales [rows][I/128]; bf16:
+ *   nearest-even; f32: as is).
+ *   xg_scales / w13_scales / hg_scales: e4m3 / e2m1 weights only, else NULL.
  *   masked_m [P+S], offsets [P+S+1]: as written by moe_permute (device).
- * bf16 / e4m3 run on the tcgen05 tensor cores and need H, I multiples of 128. */
+ * bf16 / e4m3 / e2m1 run on the tcgen05 tensor cores and need H, I multiples
+ * of 128 (e2m1: e4m3 x e2m1 products, kind::f8f6f4). */
 moe_status moe_grouped_swiglu_gemm(const moe_problem* p, const void* xg, const float* xg_scales, const void* w13,
                                    const float* w13_scales, const int32_t* masked_m, const int32_t* offsets,
                                    void* hg, float* hg_scales, int32_t* err_flag, void* workspace,

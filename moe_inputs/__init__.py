@@ -7,11 +7,14 @@ dispatch, run an expert or combine.  The CPU oracle and the CUDA path both
 read the arrays it returns.
 
 Storage conventions (shared by every consumer):
-  * bf16 arrays are ``uint16`` bit patterns; e4m3 arrays are ``uint8`` codes.
+  * bf16 arrays are ``uint16`` bit patterns; e4m3 arrays are ``uint8`` codes;
+    e2m1 (FP4) weights are ``uint8`` bytes of two codes along the reduced
+    dimension (even column in the low nibble), so their last dim is halved.
   * Expert weights are stored transposed, rows contiguous along the reduced
     dimension: ``w13 [n_exp, 2I, H]`` = gate rows (W1^T) then up rows (W3^T);
     ``w2 [n_exp, H, I]`` (W2^T).  e4m3 weights carry fp32 scales per 128x128
-    block: ``w13_s [n_exp, 2I/128, H/128]``, ``w2_s [n_exp, H/128, I/128]``.
+    block: ``w13_s [n_exp, 2I/128, H/128]``, ``w2_s [n_exp, H/128, I/128]``;
+    e2m1 weights carry the same block scales.
   * With a shared expert it is logical expert ``E`` (the last one).
 """
 from __future__ import annotations
@@ -51,6 +54,12 @@ class MoeConfig:
     w_std: float
     zipf_s: float = 0.0
     description: str = ""
+    wq: str = ""      # weight storage type when it differs from `gemm` ("e2m1": FP4 weights, e4m3 activations)
+
+    @property
+    def wt(self) -> str:
+        """Type of the stored expert weights."""
+        return self.wq or self.gemm
 
     @property
     def P(self) -> int:
@@ -108,6 +117,11 @@ CONFIGS = {
         "prefill", T=8192, H=4096, I=1024, E=512, K=10, shared=0, act="bf16", gemm="e4m3",
         out="bf16", layout="contig", M_max=0, redundant=0, router="normal", wg_std=0.0, w_std=0.02,
         description="prefill grouped layer T=8192 H=4096 I=1024 E=512 K=10, e4m3, contiguous layout"),
+    "dsv4_fp4_decode": MoeConfig(
+        "dsv4_fp4_decode", T=128, H=7168, I=2048, E=384, K=6, shared=1, act="bf16", gemm="e4m3",
+        out="bf16", layout="masked", M_max=128, redundant=0, router="normal", wg_std=0.0, w_std=0.02, wq="e2m1",
+        description="DS-V4-Pro-shaped decode layer with FP4 experts T=128 H=7168 I=2048 E=384+1 shared K=6, "
+                    "e2m1 128x128-block weights, e4m3 1x128 activations, masked [385,128,7168]"),
 }
 
 CONFIG_ORDER = ["tiny", "mixtral_decode", "dsv3_decode", "skew_eplb", "prefill"]
@@ -136,6 +150,7 @@ def _load():
         getattr(lib, name).argtypes = [u64, u64, u64, i64, dbl, dbl, vp]
         getattr(lib, name).restype = None
     lib.mg_weights_e4m3.argtypes = [u64, u64, u64, i64, i64, i64, i64, dbl, vp, vp]
+    lib.mg_weights_e2m1.argtypes = [u64, u64, u64, i64, i64, i64, i64, dbl, vp, vp]
     lib.mg_weights_bf16.argtypes = [u64, u64, i64, i64, i64, i64, dbl, vp]
     lib.mg_weights_f32.argtypes = [u64, u64, i64, i64, i64, i64, dbl, vp]
     lib.mg_num_threads.restype = ctypes.c_int
@@ -177,7 +192,7 @@ def bf16_bits_to_f64(u16: np.ndarray) -> np.ndarray:
 def expert_weights(cfg: MoeConfig, which: str, e0: int = 0, ne: int | None = None, seed: int = 0):
     """Weights of logical experts [e0, e0+ne) of ``w13`` or ``w2``.
 
-    Returns (data, scales); scales is None unless cfg.gemm == 'e4m3'."""
+    Returns (data, scales); scales is None unless the weights are e4m3 or e2m1."""
     lib = _load()
     ne = cfg.n_exp - e0 if ne is None else ne
     if which == "w13":
@@ -186,6 +201,11 @@ def expert_weights(cfg: MoeConfig, which: str, e0: int = 0, ne: int | None = Non
         N, Kd, ws, ss = cfg.H, cfg.I, STREAM_W2, STREAM_W2S
     else:
         raise ValueError(which)
+    if cfg.wt == "e2m1":
+        q = np.empty((ne, N, Kd // 2), np.uint8)
+        s = np.empty((ne, N // 128, Kd // 128), np.float32)
+        lib.mg_weights_e2m1(seed, ws, ss, e0, ne, N, Kd, cfg.w_std, q.ctypes.data, s.ctypes.data)
+        return q, s
     if cfg.gemm == "e4m3":
         q = np.empty((ne, N, Kd), np.uint8)
         s = np.empty((ne, N // 128, Kd // 128), np.float32)

@@ -132,6 +132,22 @@ static uint8_t pack_e4m3(double v) {
   return sign | (uint8_t)(((ex + 7) << 3) | man);
 }
 
+/* Encode a double as OCP FP4 E2M1 (sign, 2 exponent bits with bias 1, 1
+ * mantissa bit; magnitudes 0, 0.5, 1, 1.5, 2, 3, 4, 6): the nearest
+ * magnitude, ties to the code with mantissa bit 0, saturating to +-6. */
+static uint8_t pack_e2m1(double v) {
+  static const double mag[8] = {0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0};
+  const uint8_t sign = (v < 0) ? 0x8 : 0x0;
+  const double a = fabs(v);
+  if (a != a) return 0;
+  int best = 0;
+  for (int c = 1; c < 8; ++c) {
+    const double d = fabs(mag[c] - a), bd = fabs(mag[best] - a);
+    if (d < bd || (d == bd && (c & 1) == 0)) best = c;
+  }
+  return sign | (uint8_t)best;
+}
+
 /* ---- public entry points ---- */
 
 void mg_uniform_f64(uint64_t seed, uint64_t stream, uint64_t offset, int64_t n, double lo, double hi,
@@ -219,6 +235,48 @@ void mg_weights_e4m3(uint64_t seed, uint64_t w_stream, uint64_t s_stream, int64_
       for (int64_t i = 0; i < 128; ++i) {
         uint8_t* dst = q + (el * N + nb * 128 + i) * K + kb * 128;
         for (int64_t j = 0; j < 128; ++j) dst[j] = pack_e4m3(buf[i * 128 + j] / (double)sc);
+      }
+    }
+    free(buf);
+  }
+}
+
+/* Expert weights in FP4 E2M1 with one fp32 scale per 128x128 block: the
+ * e4m3 recipe above with the E2M1 maximum, s = fp32(u * max|w| / 6) and
+ * q = e2m1(w / s) nearest (ties to an even mantissa), saturated to +-6.
+ * Same draw indices as mg_weights_e4m3.  q is [ne, N, K/2] bytes, two codes
+ * per byte along K: column 2j in bits 0-3, column 2j+1 in bits 4-7. */
+void mg_weights_e2m1(uint64_t seed, uint64_t w_stream, uint64_t s_stream, int64_t e0, int64_t ne, int64_t N,
+                     int64_t K, double std, uint8_t* q, float* s) {
+  const uint64_t wkey = mg_stream_key(seed, w_stream);
+  const uint64_t skey = mg_stream_key(seed, s_stream);
+  const int64_t NB = N / 128, KB = K / 128;
+  const int64_t nblocks = ne * NB * KB;
+#pragma omp parallel
+  {
+    double* buf = (double*)malloc(128 * 128 * sizeof(double));
+#pragma omp for schedule(dynamic, 4)
+    for (int64_t b = 0; b < nblocks; ++b) {
+      const int64_t el = b / (NB * KB);
+      const int64_t nb = (b / KB) % NB;
+      const int64_t kb = b % KB;
+      const int64_t e = e0 + el;
+      double amax = 0.0;
+      for (int64_t i = 0; i < 128; ++i) {
+        const uint64_t base = (uint64_t)((e * N + nb * 128 + i) * K + kb * 128);
+        fill_normal(wkey, base, 128, 0.0, std, buf + i * 128);
+        for (int64_t j = 0; j < 128; ++j)
+          if (fabs(buf[i * 128 + j]) > amax) amax = fabs(buf[i * 128 + j]);
+      }
+      const double u = 0.5 + 1.5 * draw_uniform(skey, (uint64_t)((e * NB + nb) * KB + kb));
+      float sc = (float)(u * amax / 6.0);
+      if (sc == 0.0f) sc = 1.0f;
+      s[(el * NB + nb) * KB + kb] = sc;
+      for (int64_t i = 0; i < 128; ++i) {
+        uint8_t* dst = q + ((el * N + nb * 128 + i) * K + kb * 128) / 2;
+        for (int64_t j = 0; j < 128; j += 2)
+          dst[j / 2] = (uint8_t)(pack_e2m1(buf[i * 128 + j] / (double)sc) |
+                                 (pack_e2m1(buf[i * 128 + j + 1] / (double)sc) << 4));
       }
     }
     free(buf);

@@ -19,7 +19,7 @@ _HERE = os.path.dirname(os.path.abspath(__file__))
 _LIB_PATH = os.path.join(_HERE, "liboracle.so")
 _lib = None
 
-DT = {"f32": 0, "bf16": 1, "e4m3": 2}
+DT = {"f32": 0, "bf16": 1, "e4m3": 2, "e2m1": 3}
 
 
 class _Mat(ctypes.Structure):
@@ -48,6 +48,8 @@ def _load():
     mp = ctypes.POINTER(_Mat)
     lib.orc_e4m3_decode.argtypes = [ctypes.c_uint8]
     lib.orc_e4m3_decode.restype = dbl
+    lib.orc_e2m1_decode.argtypes = [ctypes.c_uint8]
+    lib.orc_e2m1_decode.restype = dbl
     lib.orc_e4m3_encode.argtypes = [ctypes.c_float]
     lib.orc_e4m3_encode.restype = ctypes.c_uint8
     lib.orc_bf16_encode.argtypes = [dbl]
@@ -90,6 +92,23 @@ def e4m3_decode(codes) -> np.ndarray:
     return out
 
 
+def e2m1_decode(codes) -> np.ndarray:
+    """Values of 4-bit E2M1 codes (one code per array element, 0..15)."""
+    codes = np.asarray(codes)
+    lib = _load()
+    table = np.array([lib.orc_e2m1_decode(c) for c in range(16)], np.float64)
+    return table[codes.astype(np.int64) & 15]
+
+
+def e2m1_decode_packed(data) -> np.ndarray:
+    """Values of packed E2M1 bytes [..., n] -> [..., 2n] (even column = low nibble)."""
+    b = np.asarray(data, np.uint8)
+    out = np.empty(b.shape[:-1] + (2 * b.shape[-1],), np.float64)
+    out[..., 0::2] = e2m1_decode(b & 15)
+    out[..., 1::2] = e2m1_decode(b >> 4)
+    return out
+
+
 def e4m3_encode(values) -> np.ndarray:
     v = _c(values, np.float32)
     out = np.empty(v.shape, np.uint8)
@@ -122,9 +141,10 @@ def quant_rows_e4m3(x) -> tuple[np.ndarray, np.ndarray]:
 # ---- matrices --------------------------------------------------------------
 
 def _mat(data, dtype: str, scales=None, scale_rows: int = 1, keep=None):
-    """A 2-D view (rows = product of leading dims) of a stored tensor."""
-    cols = data.shape[-1]
-    rows = data.size // cols
+    """A 2-D view (rows = product of leading dims) of a stored tensor (e2m1:
+    packed, the logical row is twice the stored last dim)."""
+    cols = data.shape[-1] * (2 if dtype == "e2m1" else 1)
+    rows = data.size // data.shape[-1]
     m = _Mat(DT[dtype], scale_rows, data.ctypes.data, 0 if scales is None else scales.ctypes.data, rows, cols)
     if keep is not None:
         keep.extend([data, scales])
@@ -132,7 +152,7 @@ def _mat(data, dtype: str, scales=None, scale_rows: int = 1, keep=None):
 
 
 def _np_dtype(dtype: str):
-    return {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8}[dtype]
+    return {"f32": np.float32, "bf16": np.uint16, "e4m3": np.uint8, "e2m1": np.uint8}[dtype]
 
 
 def dequant(data, dtype: str, scales=None, scale_rows: int = 1) -> np.ndarray:
@@ -141,7 +161,7 @@ def dequant(data, dtype: str, scales=None, scale_rows: int = 1) -> np.ndarray:
         return np.asarray(data, np.float64)
     if dtype == "bf16":
         return bf16_decode(data)
-    v = e4m3_decode(data)
+    v = e2m1_decode_packed(data) if dtype == "e2m1" else e4m3_decode(data)
     shp = v.shape
     v2 = v.reshape(-1, shp[-1])
     s = np.asarray(scales, np.float64).reshape(-1, shp[-1] // 128)
@@ -230,9 +250,9 @@ def grouped_swiglu(cfg, xg, xg_s, w13, w13_s, masked_m, offsets):
     w13: slot-indexed [P+S, 2I, H]."""
     keep = []
     masked = 1 if cfg.layout == "masked" else 0
-    gd = cfg.gemm
+    gd, wd = cfg.gemm, cfg.wt
     xg_m = _mat(_c(xg, _np_dtype(gd)), gd, None if xg_s is None else _c(xg_s, np.float32), 1, keep)
-    w_m = _mat(_c(w13, _np_dtype(gd)), gd, None if w13_s is None else _c(w13_s, np.float32), 128, keep)
+    w_m = _mat(_c(w13, _np_dtype(wd)), wd, None if w13_s is None else _c(w13_s, np.float32), 128, keep)
     mm = _c(masked_m, np.int32)
     off = _c(offsets, np.int32)
     hg = np.zeros((cfg.rows, cfg.I), _np_dtype(cfg.h_dtype))
@@ -247,9 +267,9 @@ def grouped_down(cfg, hg, hg_s, w2, w2_s, masked_m, offsets):
     """a4 over the grouped layout; returns yg [rows, H] in cfg.y_dtype."""
     keep = []
     masked = 1 if cfg.layout == "masked" else 0
-    gd = cfg.gemm
+    gd, wd = cfg.gemm, cfg.wt
     h_m = _mat(_c(hg, _np_dtype(gd)), gd, None if hg_s is None else _c(hg_s, np.float32), 1, keep)
-    w_m = _mat(_c(w2, _np_dtype(gd)), gd, None if w2_s is None else _c(w2_s, np.float32), 128, keep)
+    w_m = _mat(_c(w2, _np_dtype(wd)), wd, None if w2_s is None else _c(w2_s, np.float32), 128, keep)
     mm = _c(masked_m, np.int32)
     off = _c(offsets, np.int32)
     yg = np.zeros((cfg.rows, cfg.H), _np_dtype(cfg.y_dtype))
@@ -280,10 +300,10 @@ def layer(cfg, x, logits, w13, w13_s, w2, w2_s, tokens=None):
     keep = []
     T = cfg.T
     toks = np.arange(T, dtype=np.int32) if tokens is None else _c(tokens, np.int32)
-    gd = cfg.gemm
+    gd, wd = cfg.gemm, cfg.wt
     x_m = _mat(_c(x, _np_dtype(cfg.act)), cfg.act, None, 1, keep)
-    w13_m = _mat(_c(w13, _np_dtype(gd)), gd, None if w13_s is None else _c(w13_s, np.float32), 128, keep)
-    w2_m = _mat(_c(w2, _np_dtype(gd)), gd, None if w2_s is None else _c(w2_s, np.float32), 128, keep)
+    w13_m = _mat(_c(w13, _np_dtype(wd)), wd, None if w13_s is None else _c(w13_s, np.float32), 128, keep)
+    w2_m = _mat(_c(w2, _np_dtype(wd)), wd, None if w2_s is None else _c(w2_s, np.float32), 128, keep)
     lg = _c(logits, np.float32)
     out = np.zeros((toks.size, cfg.H), _np_dtype(cfg.out))
     exact = np.zeros((toks.size, cfg.H), np.float64)

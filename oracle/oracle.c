@@ -72,6 +72,17 @@ uint8_t orc_e4m3_encode(float v) {
   return sign | (uint8_t)best;
 }
 
+/* E2M1 (OCP Microscaling FP4): sign bit 3, exponent bits 2-1 with bias 1,
+ * mantissa bit 0.  E = 0 is subnormal: (M/2) * 2^0; otherwise
+ * (1 + M/2) * 2^(E-1).  No infinity or NaN: magnitudes 0, 0.5, 1, 1.5, 2, 3,
+ * 4, 6.  Used for the FP4 experts ("Inference INFRA methodology (5)",
+ * shape-evolution table, DS-V4-Pro row: native FP4). */
+double orc_e2m1_decode(uint8_t code) {
+  const int s = (code >> 3) & 1, E = (code >> 1) & 3, M = code & 1;
+  const double v = (E == 0) ? 0.5 * M : ldexp(1.0 + 0.5 * M, E - 1);
+  return s ? -v : v;
+}
+
 /* The 256 decoded E4M3 values, tabulated from orc_e4m3_decode at load time. */
 static double e4m3_table[256];
 
@@ -126,9 +137,11 @@ void orc_bf16_encode_array(int64_t n, const double* v, uint16_t* out) {
 /* Matrix views over the storage formats                                     */
 /* ------------------------------------------------------------------------ */
 
-enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2 };
+enum { ORC_F32 = 0, ORC_BF16 = 1, ORC_E4M3 = 2, ORC_E2M1 = 3 };
 
-/* rows x cols, row-major.  E4M3 data carries fp32 scales, one per
+/* rows x cols, row-major.  E2M1 data is packed two codes per byte along a
+ * row (column 2j in bits 0-3 of byte j, column 2j+1 in bits 4-7), so a row
+ * is cols/2 bytes.  E4M3 and E2M1 data carry fp32 scales, one per
  * (scale_rows x 128) block: [rows/scale_rows][cols/128].  scale_rows is 128
  * for expert weights (128x128 blocks) and 1 for activations (1x128 groups). */
 typedef struct {
@@ -146,6 +159,11 @@ static double mat_at(const orc_mat* m, int64_t r, int64_t c) {
       return (double)((const float*)m->data)[i];
     case ORC_BF16:
       return orc_bf16_decode(((const uint16_t*)m->data)[i]);
+    case ORC_E2M1: {
+      const uint8_t byte = ((const uint8_t*)m->data)[r * (m->cols / 2) + c / 2];
+      const double s = (double)m->scales[(r / m->scale_rows) * (m->cols / 128) + c / 128];
+      return orc_e2m1_decode((c & 1) ? (uint8_t)(byte >> 4) : (uint8_t)(byte & 15)) * s;
+    }
     default: {
       const double s = (double)m->scales[(r / m->scale_rows) * (m->cols / 128) + c / 128];
       return e4m3_table[((const uint8_t*)m->data)[i]] * s;

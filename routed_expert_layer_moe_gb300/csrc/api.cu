@@ -91,7 +91,7 @@ int check_problem(const moe_problem* p) {
     if (q.M_max <= 0) return MOE_ERR_INVALID;
     if (q.has_shared && q.M_max < q.T) return MOE_ERR_INVALID;
   }
-  if (q.act < MOE_F32 || q.act > MOE_E4M3 || q.wt < MOE_F32 || q.wt > MOE_E4M3 || q.out < MOE_F32 ||
+  if (q.act < MOE_F32 || q.act > MOE_E4M3 || q.wt < MOE_F32 || q.wt > MOE_E2M1 || q.out < MOE_F32 ||
       q.out > MOE_E4M3)
     return MOE_ERR_INVALID;
   // products that must fit the 32-bit row and element indices used on the device
@@ -101,7 +101,7 @@ int check_problem(const moe_problem* p) {
   // supported dtype combinations
   const bool f32 = q.act == MOE_F32 && q.wt == MOE_F32 && q.out == MOE_F32;
   const bool bf16 = q.act == MOE_BF16 && q.wt == MOE_BF16 && q.out == MOE_BF16;
-  const bool f8 = q.act == MOE_BF16 && q.wt == MOE_E4M3 && q.out == MOE_BF16;
+  const bool f8 = q.act == MOE_BF16 && fp8_acts(q) && q.out == MOE_BF16;  // FP8 or FP4 weights
   if (!(f32 || bf16 || f8)) return MOE_ERR_UNSUPPORTED;
   if (f32 && (q.H % 4 || q.I % 4)) return MOE_ERR_UNSUPPORTED;
   if ((bf16 || f8) && (q.H % 128 || q.I % 128)) return MOE_ERR_UNSUPPORTED;
@@ -182,7 +182,7 @@ moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, 
   if (r) return (moe_status)r;
   if (!masked_m || !offsets || !err_flag || !workspace) return MOE_ERR_INVALID;
   if (p->T > 0 && (!ids || !x || !row_of || !src_of || !xg)) return MOE_ERR_INVALID;
-  if (p->wt == MOE_E4M3 && p->T > 0 && !xg_scales) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && p->T > 0 && !xg_scales) return MOE_ERR_INVALID;
   if (!phys_to_log && p->P != p->E) return MOE_ERR_INVALID;
   if (p->T > 0 && (!aligned16(x) || !aligned16(xg))) return MOE_ERR_UNSUPPORTED;
   if (workspace_bytes < ws_bytes(*p)) return MOE_ERR_WORKSPACE;
@@ -197,9 +197,11 @@ static moe_status gemm_call(const moe_problem* p, int mode, const void* act, con
   int r = check_problem(p);
   if (r) return (moe_status)r;
   if (!act || !w || !masked_m || !offsets || !out || !err_flag) return MOE_ERR_INVALID;
-  if (p->wt == MOE_E4M3 && (!act_scales || !w_scales)) return MOE_ERR_INVALID;
-  if (p->wt == MOE_E4M3 && mode == MODE_SWIGLU && !out_scales) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && (!act_scales || !w_scales)) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && mode == MODE_SWIGLU && !out_scales) return MOE_ERR_INVALID;
   if (!aligned16(act) || !aligned16(w) || !aligned16(out)) return MOE_ERR_UNSUPPORTED;
+  // packed 4-bit tensor maps want a 32-byte aligned base
+  if (p->wt == MOE_E2M1 && (reinterpret_cast<uintptr_t>(w) & 31u)) return MOE_ERR_UNSUPPORTED;
   if (workspace_bytes < ws_bytes(*p) || (ws_bytes(*p) > 0 && !workspace)) return MOE_ERR_WORKSPACE;
   return launched(launch_gemm(*p, mode, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err_flag,
                               workspace, (cudaStream_t)stream));

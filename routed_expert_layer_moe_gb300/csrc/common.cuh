@@ -53,6 +53,9 @@ inline int64_t grouped_rows(const moe_problem& p) {
                                        : (int64_t)p.T * p.K + (int64_t)p.has_shared * p.T;
 }
 
+// Grouped activations (Xg, Hg) are e4m3 with 1x128 scales for FP8 and FP4 experts.
+inline bool fp8_acts(const moe_problem& p) { return p.wt == MOE_E4M3 || p.wt == MOE_E2M1; }
+
 inline size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
 
 // ---------------------------------------------------------------------------
@@ -126,6 +129,20 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   }
   return true;
 }
+
+// ---- cp.async (asynchronous global -> shared copies) ----
+
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(smem_dst)), "l"(gmem_src) : "memory");
+}
+
+// One arrival on `bar` once every cp.async this thread issued before has landed
+// (counts as one of the barrier's expected arrivals).
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // ---- TMA ----
 

@@ -59,7 +59,8 @@ constexpr int EPI_WARP0 = 4;
 constexpr int EPI_WARPS = EPI_THREADS / 32;  // epilogue barriers take one arrival per warp
 constexpr int LOAD_WARP0 = 2;       // warps 2 and 3 load FP8 scales
 constexpr int LOAD_THREADS = 64;
-constexpr int RING = 8;             // K blocks of scales staged ahead of the epilogue
+constexpr int RING = 32;            // K blocks of scales staged ahead of the epilogue
+constexpr int SG = 16;              // K blocks of scales fetched per loader pass
 // Register split (setmaxnreg): warpgroup 0 (TMA, MMA, scale loads) gives
 // registers to the two epilogue warpgroups, which hold 2 x 64 fp32
 // accumulators per thread.  4*32*ctrl + 8*32*epi must not exceed
@@ -70,7 +71,7 @@ struct Regs {
   static constexpr int epi = F8 ? 216 : 208;
   static constexpr int needed = 4 * 32 * ctrl + 8 * 32 * epi;
 };
-constexpr uint32_t TMEM_COLS = 512;
+constexpr uint32_t TMEM_COLS = 512;  // two accumulator buffers of 256 columns
 // Bound of every wait: 4e9 SM cycles, about 2 s at the 2.07 GHz maximum clock.
 constexpr long long TIMEOUT = 4000000000LL;
 
@@ -85,6 +86,8 @@ struct TcParams {
   int a1_off;        // row of the second tile of a pair relative to the first
   int out_cols;      // columns of the output rows
   int scale_cols;    // K / 128 (e4m3 scales per row of weights and activations)
+  uint32_t a_tile_tx;  // bytes one 128-row weight tile adds to its stage's transaction count
+  uint32_t w_fmt;      // kind::f8f6f4 format of the weight operand (0 = e4m3, 5 = e2m1)
   int stages;
   const int32_t* masked_m;
   const int32_t* offsets;
@@ -159,7 +162,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
                            const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
                            const __grid_constant__ CUtensorMap tmB128, const TcParams p) {
-  static_assert(TM || !F8, "FP8 runs token-major");
+  static_assert(TM || !F8, "FP8 / FP4 run token-major");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [RING][BN] activation scales of one K block
@@ -263,7 +266,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               box = 64;
             }
           }
-          const uint32_t bytes = TILE_A_BYTES * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
+          const uint32_t bytes = p.a_tile_tx * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
           for (int kb = U.kb0; kb < U.kb1; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT)) {
               ok = false;
@@ -306,7 +309,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Unit U = decode_unit<MODE>(p, prefix, u);
           // weight-major: M = 128 weight rows, N = tokens rounded to 16 (one MMA per tile);
           // token-major: M = 128 token rows, N = both weight tiles (one MMA)
-          const uint32_t idesc = TM ? mma_idesc<F8>(BM, U.a1 ? 2 * BM : BM)
+          // (token-major: the weights are the B operand, of format w_fmt)
+          const uint32_t idesc = TM ? (mma_idesc<F8>(BM, U.a1 ? 2 * BM : BM) | (p.w_fmt << 10))
                                     : mma_idesc<F8>(BM, (U.nvalid + 15) & ~15);
           uint32_t b = 0;
           if constexpr (!F8) {
@@ -373,16 +377,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     } else if (F8) {
       // ------------------------------------------------------------ FP8 scale loaders
-      // Fill the scale ring K block by K block, four blocks per pass: one thread per token
-      // row reads the row's four scales with one 16-byte load (or four scalar loads).
+      // Fill the scale ring SG K blocks per pass with asynchronous 4-byte copies: the
+      // loaders never wait for data, so the ring runs up to RING blocks ahead of the
+      // epilogue.  Each slot's rfull barrier completes when the copies issued before
+      // its arrival by all loader threads have landed.
       const int lt = tid - LOAD_WARP0 * 32;
       uint32_t g = 0;  // K blocks staged so far
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
         const Unit U = decode_unit<MODE>(p, prefix, u);
         const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
-        for (int k0 = U.kb0; ok && k0 < U.kb1; k0 += 4) {
-          const int nk = min(4, U.kb1 - k0);
+        for (int k0 = U.kb0; ok && k0 < U.kb1; k0 += SG) {
+          const int nk = min(SG, U.kb1 - k0);
           for (int j = 0; j < nk; ++j) {
             const uint32_t gj = g + j;
             if (!mbar_wait(&rempty[gj % RING], ((gj / RING) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
@@ -391,34 +397,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           if (!ok) break;
-          for (int c = lt; c < U.nvalid; c += LOAD_THREADS) {
-            const float* src = p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + k0;
-            float v[4];
-            if (nk == 4 && (reinterpret_cast<uintptr_t>(src) & 15u) == 0) {
-              const float4 f = __ldg(reinterpret_cast<const float4*>(src));
-              v[0] = f.x;
-              v[1] = f.y;
-              v[2] = f.z;
-              v[3] = f.w;
-            } else {
-#pragma unroll
-              for (int j = 0; j < 4; ++j) v[j] = (j < nk) ? __ldg(src + j) : 0.0f;
-            }
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-              if (j < nk) sx[((g + j) % RING) * BN + c] = v[j];
+          // activation scales of the chunk's rows: element (c, j) = b_scales[rowB + c][k0 + j]
+          const int n = U.nvalid * nk;
+          for (int idx = lt; idx < n; idx += LOAD_THREADS) {
+            const int c = idx / nk, j = idx - c * nk;
+            cp_async4(sx + ((g + j) % RING) * BN + c, p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + k0 + j);
           }
-          if (lt < 2 * nk) {
-            const int j = lt >> 1, t = lt & 1;
-            float w = 0.0f;
-            if (t == 0) w = __ldg(p.a_scales + (size_t)ra0 * p.scale_cols + k0 + j);
-            else if (U.a1) w = __ldg(p.a_scales + (size_t)ra1 * p.scale_cols + k0 + j);
-            sw[((g + j) % RING) * 2 + t] = w;
+          // weight block scales of the two tiles (a missing second tile's value is never used)
+          for (int idx = lt; idx < 2 * nk; idx += LOAD_THREADS) {
+            const int j = idx >> 1, t = idx & 1;
+            if (t == 0 || U.a1)
+              cp_async4(sw + ((g + j) % RING) * 2 + t, p.a_scales + (size_t)(t ? ra1 : ra0) * p.scale_cols + k0 + j);
           }
-          for (int j = 0; j < nk; ++j) mbar_arrive(&rfull[(g + j) % RING]);
+          for (int j = 0; j < nk; ++j) cp_async_arrive_noinc(&rfull[(g + j) % RING]);
           g += nk;
         }
       }
+      cp_async_wait_all();  // no copy may land after the CTA has exited
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(Regs<F8>::epi));
@@ -698,17 +693,17 @@ struct Plan {
 
 Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   Plan pl{};
-  const bool f8 = p.wt == MOE_E4M3;
+  const bool f8 = fp8_acts(p);
   const int esz = f8 ? 1 : 2;
   const int K = (mode == MODE_SWIGLU) ? p.H : p.I;
   const int NA = (mode == MODE_SWIGLU) ? 2 * p.I : p.H;
   pl.kb_total = K * esz / ROW_BYTES;
   pl.nslots = p.P + p.has_shared;
   pl.pairs = (mode == MODE_SWIGLU) ? p.I / BM : (NA + 2 * BM - 1) / (2 * BM);
-  // Token-major for FP8 always: the activation scale is then one value per thread and the
-  // SwiGLU / e4m3 re-quantisation of h are row-local, which measured faster than the
-  // weight-major epilogue even for decode experts with a few tokens.  BF16 needs no
-  // promotion; there weight-major is kept for decode-sized experts.
+  // Token-major for FP8 / FP4 always: the activation scale is then one value per thread and
+  // the SwiGLU / e4m3 re-quantisation of h are row-local.  A weight-major FP8 variant (tokens
+  // as the MMA's N) measured slower even for decode experts with two to eight tokens.  BF16
+  // needs no promotion; there weight-major is kept for decode-sized experts.
   const double rows_per_slot = (double)p.T * p.K / std::max(1, p.P);
   pl.tm = f8 || rows_per_slot >= 64.0;
   // upper bound of the token chunks over all slots
@@ -803,7 +798,12 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   const uint64_t rowsB = (uint64_t)grouped_rows(p);
   const uint32_t box_k = ROW_BYTES / esz;
   CUtensorMap tA, tB[4];
-  if (encode_tensor_map(&tA, dt, K, rowsA, (uint64_t)K * esz, box_k, BM, w) != CUDA_SUCCESS) return MOE_ERR_CUDA;
+  // e2m1 weights: packed 4-bit rows of K/2 bytes; TMA spreads each 8 bytes of codes over
+  // 16 bytes of shared memory (the layout kind::f8f6f4 reads) and counts the 8 bytes read
+  const bool w4 = p.wt == MOE_E2M1;
+  if (encode_tensor_map(&tA, w4 ? CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B : dt, K, rowsA,
+                        w4 ? (uint64_t)K / 2 : (uint64_t)K * esz, box_k, BM, w) != CUDA_SUCCESS)
+    return MOE_ERR_CUDA;
   const int boxes[4] = {16, 32, 64, 128};
   for (int i = 0; i < 4; ++i)
     if (encode_tensor_map(&tB[i], dt, K, rowsB, (uint64_t)K * esz, box_k, boxes[i], act) != CUDA_SUCCESS)
@@ -822,6 +822,8 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   prm.a1_off = (MODE == MODE_SWIGLU) ? p.I : BM;
   prm.out_cols = (MODE == MODE_SWIGLU) ? p.I : p.H;
   prm.scale_cols = K / 128;
+  prm.a_tile_tx = w4 ? TILE_A_BYTES / 2 : TILE_A_BYTES;
+  prm.w_fmt = w4 ? 5u : 0u;
   prm.stages = pl.stages;
   prm.masked_m = masked_m;
   prm.offsets = offsets;
@@ -943,7 +945,7 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
   const DeviceInfo& di = device_info();
   const Plan pl = make_plan(p, mode, di.sm_count, di.max_smem_optin);
   if (pl.stages == 0) return MOE_ERR_UNSUPPORTED;
-  const bool f8 = p.wt == MOE_E4M3;
+  const bool f8 = fp8_acts(p);
 #define MOE_LAUNCH(F8_, MODE_, TM_)                                                                              \
   return launch_tc<F8_, MODE_, TM_>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err, \
                                     ws, st)

@@ -284,7 +284,7 @@ int launch_permute(const moe_problem& p, const int32_t* ids, const void* x, cons
   scan_kernel<<<1, 1024, 0, st>>>(w.bits, W, p.P, p.has_shared, p.T, masked, p.M_max, w.prefix, masked_m, offsets,
                                   err);
   if (p.T > 0) {
-    if (p.wt == MOE_E4M3) {
+    if (fp8_acts(p)) {
       scatter_kernel<__nv_bfloat16, true><<<p.T, 256, 0, st>>>(
           (const __nv_bfloat16*)x, p.H, p.T, p.K, p.P, p.has_shared, masked, p.M_max, w.bits, w.prefix, W,
           w.slot_of, offsets, row_of, src_of, xg, xg_scales);

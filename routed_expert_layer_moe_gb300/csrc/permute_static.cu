@@ -71,7 +71,7 @@ extern "C" moe_status moe_permute_no_workspace(const moe_problem* p, const int32
   if (st != MOE_OK) return st;
   if (!masked_m || !offsets || !err_flag) return MOE_ERR_INVALID;
   if (p->T > 0 && (!ids || !x || !row_of || !src_of || !xg)) return MOE_ERR_INVALID;
-  if (p->wt == MOE_E4M3 && p->T > 0 && !xg_scales) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && p->T > 0 && !xg_scales) return MOE_ERR_INVALID;
   if (!phys_to_log && p->P != p->E) return MOE_ERR_INVALID;
   if (p->T > 0 && (!aligned16(x) || !aligned16(xg))) return MOE_ERR_UNSUPPORTED;
   // the scratch this problem needs must fit in the fixed array

@@ -76,37 +76,47 @@ void launch_route_per(const moe_problem& p, const float* logits, int32_t* ids, f
 // sigmoid scores, e_score_correction_bias used for the choice only, grouped
 // top-k (the best topk_group of n_group contiguous expert groups, a group
 // scored by its best biased score, then the K best experts inside them).  The
-// keys are compared in fp64 (ties to the lower index); weights are the unbiased
-// scores of the chosen experts, renormalised if asked, times `scale`.
-template <int PER>
-__global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restrict__ logits,
-                                                            const float* __restrict__ bias, int T, int E, int K,
-                                                            int n_group, int topk_group, int renorm, float scale,
-                                                            int32_t* __restrict__ ids, float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
-  const int t = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
-  if (t >= T) return;
+// keys are formed and compared in fp64 (ties to the lower index); weights are
+// the unbiased scores of the chosen experts, renormalised if asked, times
+// `scale`.  One CTA per token: its 128 threads evaluate the E fp64 sigmoids
+// (fp64 throughput is low, so they are spread over the whole CTA), then warp 0
+// makes the choices from shared memory.
+constexpr int GROUPED_THREADS = 128;
+
+template <int PER>  // keys held per lane of warp 0: E <= 32 * PER
+__global__ void __launch_bounds__(GROUPED_THREADS) route_grouped_kernel(const float* __restrict__ logits,
+                                                                        const float* __restrict__ bias, int T, int E,
+                                                                        int K, int n_group, int topk_group,
+                                                                        int renorm, float scale,
+                                                                        int32_t* __restrict__ ids,
+                                                                        float* __restrict__ w) {
+  __shared__ double s_sc[1024], s_key[1024];
+  const int t = blockIdx.x;
   const float* l = logits + (size_t)t * E;
+  for (int e = threadIdx.x; e < E; e += GROUPED_THREADS) {
+    const double sc = 1.0 / (1.0 + exp(-(double)__ldg(l + e)));
+    s_sc[e] = sc;
+    s_key[e] = sc + (bias ? (double)__ldg(bias + e) : 0.0);
+  }
+  __syncthreads();
+  if (threadIdx.x >= 32) return;
+  const int lane = threadIdx.x;
   const int gs = E / n_group;
-  double sc[PER], key[PER];
+  double key[PER];
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
-    sc[i] = 0.0;
-    key[i] = -INFINITY;
-    if (e < E) {
-      sc[i] = 1.0 / (1.0 + exp(-(double)__ldg(l + e)));
-      key[i] = sc[i] + (bias ? (double)__ldg(bias + e) : 0.0);
-    }
+    key[i] = (e < E) ? s_key[e] : -INFINITY;
   }
   // group maxima: lane g keeps the score of group g
   double gmine = -INFINITY;
   for (int g = 0; g < n_group; ++g) {
     double m = -INFINITY;
+    const int e_lo = g * gs, e_hi = e_lo + gs;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
-      if (e < E && e / gs == g) m = fmax(m, key[i]);
+      if (e >= e_lo && e < e_hi) m = fmax(m, key[i]);
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, off));
@@ -115,8 +125,9 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restr
   // the topk_group best groups (ties to the lower group index)
   uint32_t gsel = 0;
   for (int r = 0; r < topk_group; ++r) {
-    double bv = (lane < n_group && !((gsel >> lane) & 1u)) ? gmine : -INFINITY;
-    int bg = (lane < n_group && !((gsel >> lane) & 1u)) ? lane : 0x7fffffff;
+    const bool cand = lane < n_group && !((gsel >> lane) & 1u);
+    double bv = cand ? gmine : -INFINITY;
+    int bg = cand ? lane : 0x7fffffff;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
@@ -135,16 +146,14 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restr
     if (e < E && ((gsel >> (e / gs)) & 1u)) avail |= 1u << i;
   }
   int my_id = 0;
-  double my_sc = 0.0;
   for (int k = 0; k < K; ++k) {
-    double bv = -INFINITY, bs = 0.0;
+    double bv = -INFINITY;
     int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       if ((avail >> i) & 1u) {
         if (be == 0x7fffffff || key[i] > bv) {
           bv = key[i];
-          bs = sc[i];
           be = lane + 32 * i;
         }
       }
@@ -152,20 +161,16 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restr
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
       const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const double os = __shfl_xor_sync(0xffffffffu, bs, off);
       const int oe = __shfl_xor_sync(0xffffffffu, be, off);
       if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
         bv = ov;
-        bs = os;
         be = oe;
       }
     }
     if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
-    if (lane == k) {
-      my_id = be;
-      my_sc = bs;
-    }
+    if (lane == k) my_id = be;
   }
+  const double my_sc = (lane < K) ? s_sc[my_id] : 0.0;
   double sum = 0.0;
   for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, my_sc, k);  // fixed order
   if (lane < K) {
@@ -177,10 +182,8 @@ __global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restr
 template <int PER>
 void launch_grouped_per(const moe_problem& p, const float* logits, const float* bias, int n_group, int topk_group,
                         int renorm, float scale, int32_t* ids, float* w, cudaStream_t st) {
-  const int threads = 256;
-  const int blocks = (int)(((int64_t)p.T * 32 + threads - 1) / threads);
-  route_grouped_kernel<PER><<<blocks, threads, 0, st>>>(logits, bias, p.T, p.E, p.K, n_group, topk_group, renorm,
-                                                        scale, ids, w);
+  route_grouped_kernel<PER><<<p.T, GROUPED_THREADS, 0, st>>>(logits, bias, p.T, p.E, p.K, n_group, topk_group,
+                                                             renorm, scale, ids, w);
 }
 
 }  // namespace

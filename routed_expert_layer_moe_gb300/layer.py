@@ -9,13 +9,15 @@ import torch
 
 from . import _lib as L
 
-TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8}
+TORCH_DTYPE = {"f32": torch.float32, "bf16": torch.bfloat16, "e4m3": torch.uint8, "e2m1": torch.uint8}
 
 
 class MoeLayer:
     """Buffers and calls for one problem.  Weights are slot-indexed tensors on the
     device: w13 [P+S, 2I, H], w2 [P+S, H, I] (e4m3: uint8 codes with fp32 block
-    scales w13_s [P+S, 2I/128, H/128], w2_s [P+S, H/128, I/128])."""
+    scales w13_s [P+S, 2I/128, H/128], w2_s [P+S, H/128, I/128]; e2m1: the same
+    with two codes per byte, w13 [P+S, 2I, H/2], w2 [P+S, H, I/2]).  With e4m3
+    or e2m1 weights the grouped activations xg, hg are e4m3 with 1x128 scales."""
 
     def __init__(self, problem: L.Problem, act: str, wt: str, out: str, w13, w2, w13_s=None, w2_s=None,
                  phys_to_log=None, device="cuda"):
@@ -38,12 +40,12 @@ class MoeLayer:
         self.offsets = torch.empty(p.P + S + 1, **i32)
         self.row_of = torch.empty((p.T, p.K + S), **i32)
         self.src_of = torch.full((rows,), -1, **i32)
+        f8 = wt in ("e4m3", "e2m1")
         gd = TORCH_DTYPE[wt]
         yd = torch.float32 if wt == "f32" else torch.bfloat16
         self.xg = torch.empty((rows, p.H), dtype=gd, device=dev)
         self.hg = torch.empty((rows, p.I), dtype=gd, device=dev)
         self.yg = torch.empty((rows, p.H), dtype=yd, device=dev)
-        f8 = wt == "e4m3"
         self.xg_s = torch.empty((rows, p.H // 128), dtype=torch.float32, device=dev) if f8 else None
         self.hg_s = torch.empty((rows, p.I // 128), dtype=torch.float32, device=dev) if f8 else None
         self.out = torch.empty((p.T, p.H), dtype=TORCH_DTYPE[out], device=dev)
@@ -54,6 +56,11 @@ class MoeLayer:
     # -- the steps --------------------------------------------------------------
     def route(self, logits, stream=None):
         L.moe_route_topk(self.p, logits, self.ids, self.w, stream)
+
+    def route_grouped(self, logits, n_group, topk_group, bias=None, renormalize=True, scale=1.0, stream=None):
+        """DeepSeek-style grouped top-k (sigmoid, bias for the choice only) in place of route()."""
+        L.moe_route_grouped_topk(self.p, logits, bias, n_group, topk_group, self.ids, self.w,
+                                 renormalize=renormalize, scale=scale, stream=stream)
 
     def permute(self, x, stream=None):
         L.moe_permute(self.p, self.ids, x, self.p2l, self.masked_m, self.offsets, self.row_of, self.src_of,

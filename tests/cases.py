@@ -21,4 +21,9 @@ SMALL = {
         name="e4m3_contig_tm", T=320, H=384, I=256, E=5, K=2),
     "bf16_masked_tm": CONFIGS["mixtral_decode"].replace(
         name="bf16_masked_tm", T=200, H=256, I=384, E=4, K=2, M_max=200),
+    # FP4 (e2m1) experts: the decode shape with a shared expert, and a prefill-sized contiguous one
+    "e2m1_masked_shared": CONFIGS["dsv4_fp4_decode"].replace(
+        name="e2m1_masked_shared", T=40, H=384, I=256, E=16, K=3, M_max=40),
+    "e2m1_contig_tm": CONFIGS["dsv4_fp4_decode"].replace(
+        name="e2m1_contig_tm", T=320, H=384, I=256, E=5, K=2, shared=0, layout="contig", M_max=0),
 }

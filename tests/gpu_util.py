@@ -9,12 +9,12 @@ import moe_inputs as mi
 import oracle
 import routed_expert_layer_moe_gb300 as moe
 
-TOL = {"f32": 1e-4, "bf16": 1e-2, "e4m3": 3e-2}
+TOL = {"f32": 1e-4, "bf16": 1e-2, "e4m3": 3e-2}  # by the type of the GEMM operands (e4m3 also for e2m1 weights)
 
 
 def problem_of(cfg) -> moe.Problem:
     return moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, P=cfg.P, M_max=cfg.M_max,
-                            has_shared=cfg.S, act=cfg.act, wt=cfg.gemm, out=cfg.out, layout=cfg.layout)
+                            has_shared=cfg.S, act=cfg.act, wt=cfg.wt, out=cfg.out, layout=cfg.layout)
 
 
 def to_dev(a: np.ndarray | None, dev="cuda"):
@@ -83,5 +83,5 @@ class Workload:
     def layer(self) -> moe.MoeLayer:
         w13, w13s, w2, w2s = self.device_weights()
         p2l = None if self.p2l is None else torch.from_numpy(self.p2l).cuda()
-        return moe.MoeLayer(self.problem, self.cfg.act, self.cfg.gemm, self.cfg.out, w13, w2, w13s, w2s,
+        return moe.MoeLayer(self.problem, self.cfg.act, self.cfg.wt, self.cfg.out, w13, w2, w13s, w2s,
                             phys_to_log=p2l)

@@ -80,7 +80,7 @@ def test_layer_empty_batch():
 
 # ---- full-size workloads, sampled --------------------------------------------------------
 
-FULL = ["tiny", "mixtral_decode", "dsv3_decode", "skew_eplb", "prefill"]
+FULL = ["tiny", "mixtral_decode", "dsv3_decode", "skew_eplb", "prefill", "dsv4_fp4_decode"]
 
 
 @pytest.fixture(scope="module")

@@ -50,6 +50,25 @@ def test_e4m3_weight_recipe():
     assert abs(deq.std() - cfg.w_std) < 0.1 * cfg.w_std
 
 
+def test_e2m1_weight_recipe():
+    """FP4 weights: per 128x128 block s = u * max|w| / 6 with u in [0.5, 2], so the
+    block's largest code magnitude is e2m1(6/u): 6 when u <= 1.2 (saturated or
+    rounded up), else 3 or 4; the codes are packed two per byte; the dequantised
+    weights keep the drawn standard deviation within FP4's coarse grid."""
+    cfg = SMALL["e2m1_masked_shared"]
+    q, s = mi.expert_weights(cfg, "w13")
+    assert q.shape == (cfg.n_exp, 2 * cfg.I, cfg.H // 2) and s.shape == (cfg.n_exp, 2 * cfg.I // 128, cfg.H // 128)
+    v = oracle.dequant(q, "e2m1", np.ones_like(s), 128)
+    blocks = np.abs(v).reshape(cfg.n_exp, 2 * cfg.I // 128, 128, cfg.H // 128, 128).max(axis=(2, 4))
+    assert set(np.unique(blocks)) <= {3.0, 4.0, 6.0}
+    deq = oracle.dequant(q, "e2m1", s, 128)
+    assert abs(deq.std() - cfg.w_std) < 0.25 * cfg.w_std
+    # same draws as the e4m3 weights of the same shapes: the two dequantisations agree to FP4 precision
+    q8, s8 = mi.expert_weights(cfg.replace(wq=""), "w13")
+    d8 = oracle.dequant(q8, "e4m3", s8, 128)
+    assert np.corrcoef(deq.ravel(), d8.ravel())[0, 1] > 0.97
+
+
 def test_router_recipes():
     cfg = SMALL["e4m3_eplb_zipf"]
     _, logits = mi.activations(cfg)

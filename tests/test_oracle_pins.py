@@ -118,6 +118,66 @@ def test_e4m3_encode_rne_satfinite():
     assert tie.tolist() == [0x38, 0x3A]
 
 
+# OCP Microscaling Formats (MX) v1.0, section 5.3.3 (FP4 E2M1): exponent bias
+# 1, one mantissa bit, no Inf/NaN; the eight magnitudes as the spec lists them.
+E2M1_MAGNITUDES = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+
+def test_e2m1_decode_all_codes():
+    v = oracle.e2m1_decode(np.arange(16))
+    assert v[:8].tolist() == E2M1_MAGNITUDES
+    assert (v[8:] == -np.array(E2M1_MAGNITUDES)).all() and np.signbit(v[8])
+
+
+def test_e2m1_packed_nibble_order_and_scales():
+    """Byte j of a row holds column 2j in its low nibble; block scales index
+    [row/128][col/128]."""
+    data = np.zeros((128, 128), np.uint8)          # 128 rows x 256 columns
+    data[0, 0] = 0x71                               # col 0 = 0.5, col 1 = 6
+    data[5, 64] = 0x2F                              # col 128 = -6, col 129 = 1
+    s = np.array([[2.0, 0.25]], np.float32)         # one 128-row block, two column blocks
+    v = oracle.dequant(data, "e2m1", s, 128)
+    assert v.shape == (128, 256)
+    assert v[0, 0] == 1.0 and v[0, 1] == 12.0 and v[5, 128] == -1.5 and v[5, 129] == 0.25
+    assert np.count_nonzero(v) == 4
+
+
+def _e2m1_unpack_by_hand(q):
+    """Independent unpacking for the checks below: nibble -> sign * magnitude."""
+    mag = np.array(E2M1_MAGNITUDES)
+    lo, hi = q & 15, q >> 4
+    out = np.empty(q.shape[:-1] + (2 * q.shape[-1],))
+    out[..., 0::2] = np.where(lo & 8, -1.0, 1.0) * mag[lo & 7]
+    out[..., 1::2] = np.where(hi & 8, -1.0, 1.0) * mag[hi & 7]
+    return out
+
+
+def test_single_fp4_expert_steps_against_dense():
+    """E = 1, K = 1 with FP4 weights: gate/up and down of the oracle against numpy
+    matmuls on weights decoded by hand (scales expanded per 128x128 block)."""
+    cfg = SMALL["e2m1_masked_shared"].replace(T=6, H=256, I=128, E=1, K=1, shared=0, M_max=6)
+    x, logits = mi.activations(cfg)
+    w13, w13s = mi.expert_weights(cfg, "w13")
+    w2, w2s = mi.expert_weights(cfg, "w2")
+    ex = lambda s_: np.repeat(np.repeat(s_.astype(np.float64), 128, 0), 128, 1)
+    W13 = _e2m1_unpack_by_hand(w13[0]) * ex(w13s[0])     # [2I, H]
+    W2 = _e2m1_unpack_by_hand(w2[0]) * ex(w2s[0])        # [H, I]
+    ids, _ = oracle.route(logits, 1)
+    lay = oracle.layout(cfg, ids)
+    xg, xgs = oracle.dispatch_values(cfg, x, lay["row_of"])
+    hg, hgs = oracle.grouped_swiglu(cfg, xg, xgs, w13, w13s, lay["masked_m"], lay["offsets"])
+    xq = oracle.dequant(xg[:6], "e4m3", xgs[:6], 1)
+    g, u = xq @ W13[:128].T, xq @ W13[128:].T
+    h = _silu(g) * u
+    hq = oracle.dequant(hg[:6], "e4m3", hgs[:6], 1)
+    assert np.abs(hq - h).max() <= np.abs(h).max() / 16      # e4m3 keeps 4 significant bits
+    assert np.abs(hq - h).max() > 0
+    yg = oracle.grouped_down(cfg, hg, hgs, w2, w2s, lay["masked_m"], lay["offsets"])
+    y = hq @ W2.T
+    yb = oracle.dequant(yg[:6], "bf16")
+    assert np.abs(yb - y).max() <= 2.0 ** -8 * np.abs(y).max()
+
+
 def test_bf16_encode_rne():
     rng = np.random.default_rng(2)
     base = rng.standard_normal(50000).astype(np.float32)

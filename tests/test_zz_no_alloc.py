@@ -38,9 +38,9 @@ def outputs(L, xg_bytes_fill=0x5A):
              offsets=torch.full((p.P + p.has_shared + 1,), -7, **i32),
              row_of=torch.full((p.T, p.K + p.has_shared), -7, **i32),
              src_of=torch.full((rows,), -7, **i32),
-             xg=torch.full((rows, p.H), xg_bytes_fill, dtype=torch.uint8, device=dev) if L.wt == "e4m3"
+             xg=torch.full((rows, p.H), xg_bytes_fill, dtype=torch.uint8, device=dev) if L.wt in ("e4m3", "e2m1")
              else torch.full((rows, p.H), -3.0, dtype=L.xg.dtype, device=dev),
-             xg_s=torch.full((rows, p.H // 128), -3.0, dtype=torch.float32, device=dev) if L.wt == "e4m3" else None,
+             xg_s=torch.full((rows, p.H // 128), -3.0, dtype=torch.float32, device=dev) if L.wt in ("e4m3", "e2m1") else None,
              err=torch.zeros(1, **i32))
     return o
 
