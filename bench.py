@@ -35,8 +35,9 @@ METRIC = "MoE layer tokens/s"
 # ncu DRAM bytes (read + write) per launch of the dominant kernel, keyed by the
 # workload and the hash of the kernel source they were captured from.
 TRAFFIC = {
-    # gate/up kernel, ncu --set full (profiles/gemm_gateup_mixtral_decode.md): 1.880361 GB read + 3.809 MB written
-    "mixtral_decode:18ca0ac07d3445ad": 1884170280,
+    # one-launch gate/up + down kernel, ncu --set full (profiles/gemm_ffn_mixtral_decode.md):
+    # 2.821602 GB read + 5.709 MB written
+    "mixtral_decode:ffn:673cc1410b1c19a1": 2827311312,
 }
 
 
@@ -219,12 +220,19 @@ def run_gpu(args, cfg, rank, world, local_rank):
     stream = torch.cuda.Stream(dev)
     # eager warm-up on the capture stream (first calls cache device attributes)
     with torch.cuda.stream(stream):
-        L.forward(xd, ld, stream)
+        L.forward(xd, ld, stream, fused=not args.split_ffn)
     stream.synchronize()
     assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
 
-    parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.swiglu(stream),
-             lambda: L.down(stream), lambda: L.combine(stream)]
+    if args.split_ffn:  # gate/up and down as two launches
+        names = ["route+permute", "gate_up", "down", "combine"]
+        parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.swiglu(stream),
+                 lambda: L.down(stream), lambda: L.combine(stream)]
+    else:  # gate/up and down in one launch (moe_grouped_ffn)
+        names = ["route+permute", "gate_up+down", "combine"]
+        parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.ffn(stream),
+                 lambda: L.combine(stream)]
+    NP = len(parts)
     graphs = []
     for fn in parts:
         try:  # keep the graph itself (not only its executable) so its kernel nodes can be counted
@@ -248,7 +256,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
     stream.synchronize()
 
     K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(K)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(NP + 1)] for _ in range(K)]
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize()
@@ -262,8 +270,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
         torch.cuda.synchronize()
     if world > 1:
         torch.distributed.barrier()
-    total_ms = ev[0][0].elapsed_time(ev[K - 1][4])
-    part_ms = [statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(4)]
+    total_ms = ev[0][0].elapsed_time(ev[K - 1][NP])
+    part_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(NP)}
     if world > 1:
         t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
@@ -377,23 +385,30 @@ def count_launches(graphs, cfg, with_map):
         return 1 + 3 + (1 if with_map else 0) + 1 + 1 + 1, "static count"
 
 
-def gateup_roofline(cfg, res, peaks, moe_src):
-    """Algorithmic bytes of one gate/up launch: the W13 (+ scales) of every slot
-    with rows, the grouped activations it reads and the Hg it writes."""
+def ffn_roofline(cfg, res, peaks, moe_src, split):
+    """Roofline of the dominant kernel.  One launch of gate/up and down (default): the W13 and
+    W2 (+ scales) of every slot with rows, Xg read, Hg written and read back, Yg written; its
+    event-timed duration includes the split-K reduction kernel the same call enqueues.  With
+    --split-ffn: the gate/up launch alone (W13 + scales, Xg read, Hg written)."""
     hbm, _, _, src = peaks
-    b13, _ = expert_bytes(cfg)
-    mm = res["masked_m"]
-    rows = int(mm.sum())
+    b13, b2 = expert_bytes(cfg)
+    rows = int(res["masked_m"].sum())
     esz = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.gemm]
-    act = rows * cfg.H * esz + rows * cfg.I * esz
+    x_b, h_b = rows * cfg.H * esz, rows * cfg.I * esz
     if cfg.gemm == "e4m3":
-        act += rows * (cfg.H // 128 + cfg.I // 128) * 4
-    algo = res["touched"] * b13 + act
-    dur_s = res["part_ms"][1] * 1e-3
+        x_b += rows * (cfg.H // 128) * 4
+        h_b += rows * (cfg.I // 128) * 4
+    if split:
+        algo = res["touched"] * b13 + x_b + h_b
+        dur_s = res["part_ms"]["gate_up"] * 1e-3
+        kernel = "grouped_gemm_tc (gate/up + SwiGLU)"
+    else:
+        algo = res["touched"] * (b13 + b2) + x_b + 2 * h_b + rows * cfg.H * (4 if cfg.gemm == "f32" else 2)
+        dur_s = res["part_ms"]["gate_up+down"] * 1e-3
+        kernel = "grouped_gemm_tc, gate/up + SwiGLU + down in one launch (+ its split-K reduction)"
     achieved = algo / dur_s / 1e9
-    key = "%s:%s" % (cfg.name, moe_src)
-    traffic = TRAFFIC.get(key)
-    return {"bound": "hbm", "kernel": "grouped_gemm_tc (gate/up + SwiGLU)", "achieved": round(achieved, 1),
+    traffic = TRAFFIC.get("%s:%s:%s" % (cfg.name, "split" if split else "ffn", moe_src))
+    return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
             "peak": hbm, "unit": "GB/s", "frac": round(achieved / hbm, 4), "traffic": traffic,
             "algorithmic_bytes": int(algo), "avg_launch_us": round(dur_s * 1e6, 2), "peak_source": src}
 
@@ -462,6 +477,9 @@ def main():
     ap.add_argument("--config", default=HEADLINE, choices=list(mi.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--ffn", default="auto", choices=["auto", "fused", "split"],
+                    help="gate/up and down as one launch (moe_grouped_ffn) or two; auto: one launch for bf16 "
+                         "experts, two for e4m3 / e2m1 (the faster of the two on GB300 for each)")
     ap.add_argument("--override", default="",
                     help="comma-separated field=value changes to the workload, e.g. T=2048,E=128 (profiling cases)")
     args = ap.parse_args()
@@ -473,6 +491,7 @@ def main():
             k, v = item.split("=")
             kw[k.strip()] = type(getattr(cfg, k.strip()))(v)
         cfg = cfg.replace(name=cfg.name + "[" + args.override + "]", **kw)
+    args.split_ffn = args.ffn == "split" or (args.ffn == "auto" and cfg.gemm != "bf16")
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
@@ -499,12 +518,9 @@ def main():
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": cfg.gemm if cfg.wt == cfg.gemm else "%s x %s" % (cfg.wt, cfg.gemm),
             "data": "synthetic (seeded generator, random-init experts)",
-            "config": config_dict(cfg, world),
-            "roofline": gateup_roofline(cfg, res, peaks, moe_src),
-            "step_breakdown_us": {"route+permute": round(res["part_ms"][0] * 1e3, 2),
-                                  "gate_up": round(res["part_ms"][1] * 1e3, 2),
-                                  "down": round(res["part_ms"][2] * 1e3, 2),
-                                  "combine": round(res["part_ms"][3] * 1e3, 2)},
+            "config": dict(config_dict(cfg, world), ffn="two launches" if args.split_ffn else "one launch"),
+            "roofline": ffn_roofline(cfg, res, peaks, moe_src, args.split_ffn),
+            "step_breakdown_us": {k: round(v * 1e3, 2) for k, v in res["part_ms"].items()},
             "touched_slots": res["touched"],
             "aux_calls_us": res["aux"],
             "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],

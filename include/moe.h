@@ -234,6 +234,25 @@ moe_status moe_grouped_down_gemm(const moe_problem* p, const void* hg, const flo
                                  void* yg, int32_t* err_flag, void* workspace, size_t workspace_bytes,
                                  moe_stream_t stream);
 
+/* Steps 3 and 4 in one launch (the fused path of "MoE inference and expert
+ * parallelism", routing section: "fused MoE" runs the grouped gate/up, the
+ * activation and the grouped down GEMM as one unit of work).  Same arguments,
+ * outputs and numerics as moe_grouped_swiglu_gemm followed by
+ * moe_grouped_down_gemm (hg/hg_scales are still written; yg is bit-identical
+ * to the two separate calls).  On the tensor cores it is one persistent
+ * cooperative launch in which a CTA moves on to down tiles as soon as every
+ * gate/up tile of that slot has released its rows of h, so the down GEMM's
+ * weight streaming overlaps the end of gate/up (plus the split-K reduction
+ * kernel when the down GEMM is split); fp32 problems run the two CUDA-core
+ * GEMMs one after the other.  All CTAs must be resident at once: the launch
+ * fails (MOE_ERR_CUDA) if the device cannot co-schedule them.  workspace:
+ * moe_workspace_bytes(p) bytes (it holds the per-slot ready counters, cleared
+ * by this call). */
+moe_status moe_grouped_ffn(const moe_problem* p, const void* xg, const float* xg_scales, const void* w13,
+                           const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
+                           const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err_flag,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream);
+
 /* Step 5 (combine; "MoE inference and expert parallelism", routing section:
  * moe_sum / TopKWeightAndReduce, DeepSeek-V3 Eq. 12 for the shared expert):
  *   out[t] = sum_{k<K} w[t,k] * yg[row_of[t,k]]  (+ yg[row_of[t,K]] if S),

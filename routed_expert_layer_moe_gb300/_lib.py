@@ -23,7 +23,8 @@ LAYOUTS = {"masked": MOE_LAYOUT_MASKED, "contig": MOE_LAYOUT_CONTIG}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_version", "moe_status_string", "moe_grouped_rows", "moe_workspace_bytes", "moe_check_problem",
-           "moe_route_topk", "moe_route_grouped_topk", "moe_permute", "moe_permute_no_workspace", "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_combine",
+           "moe_route_topk", "moe_route_grouped_topk", "moe_permute", "moe_permute_no_workspace",
+           "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_grouped_ffn", "moe_combine",
            "moe_eplb_record", "moe_eplb_rebalance", "moe_eplb_invert"]
 
 
@@ -82,6 +83,8 @@ def lib():
     L.moe_grouped_swiglu_gemm.restype = i32
     L.moe_grouped_down_gemm.argtypes = [pp] + [vp] * 9 + [sz, vp]
     L.moe_grouped_down_gemm.restype = i32
+    L.moe_grouped_ffn.argtypes = [pp] + [vp] * 13 + [sz, vp]
+    L.moe_grouped_ffn.restype = i32
     L.moe_combine.argtypes = [pp, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
     L.moe_eplb_record.argtypes = [pp, vp, i64, i32, vp, vp]
@@ -178,6 +181,14 @@ def moe_grouped_down_gemm(p: Problem, hg, hg_scales, w2, w2_scales, masked_m, of
     _check(lib().moe_grouped_down_gemm(ctypes.byref(p), _ptr(hg), _ptr(hg_scales), _ptr(w2), _ptr(w2_scales),
                                        _ptr(masked_m), _ptr(offsets), _ptr(yg), _ptr(err_flag), _ptr(workspace),
                                        nbytes, _stream(stream)), "moe_grouped_down_gemm")
+
+
+def moe_grouped_ffn(p: Problem, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg, hg_scales, yg,
+                    err_flag, workspace, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().moe_grouped_ffn(ctypes.byref(p), _ptr(xg), _ptr(xg_scales), _ptr(w13), _ptr(w13_scales), _ptr(w2),
+                                 _ptr(w2_scales), _ptr(masked_m), _ptr(offsets), _ptr(hg), _ptr(hg_scales), _ptr(yg),
+                                 _ptr(err_flag), _ptr(workspace), nbytes, _stream(stream)), "moe_grouped_ffn")
 
 
 def moe_combine(p: Problem, yg, row_of, w, out, stream=None) -> None:

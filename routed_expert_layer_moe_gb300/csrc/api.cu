@@ -223,6 +223,23 @@ moe_status moe_grouped_down_gemm(const moe_problem* p, const void* hg, const flo
                    workspace_bytes, stream);
 }
 
+moe_status moe_grouped_ffn(const moe_problem* p, const void* xg, const float* xg_scales, const void* w13,
+                           const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
+                           const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err_flag,
+                           void* workspace, size_t workspace_bytes, moe_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return (moe_status)r;
+  if (!xg || !w13 || !w2 || !masked_m || !offsets || !hg || !yg || !err_flag) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && (!xg_scales || !w13_scales || !w2_scales || !hg_scales)) return MOE_ERR_INVALID;
+  if (!aligned16(xg) || !aligned16(w13) || !aligned16(w2) || !aligned16(hg) || !aligned16(yg))
+    return MOE_ERR_UNSUPPORTED;
+  if (p->wt == MOE_E2M1 && ((reinterpret_cast<uintptr_t>(w13) | reinterpret_cast<uintptr_t>(w2)) & 31u))
+    return MOE_ERR_UNSUPPORTED;
+  if (workspace_bytes < ws_bytes(*p) || (ws_bytes(*p) > 0 && !workspace)) return MOE_ERR_WORKSPACE;
+  return launched(launch_grouped_ffn(*p, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg,
+                                     hg_scales, yg, err_flag, workspace, (cudaStream_t)stream));
+}
+
 moe_status moe_combine(const moe_problem* p, const void* yg, const int32_t* row_of, const float* w, void* out,
                        moe_stream_t stream) {
   int r = check_problem(p);

@@ -39,6 +39,10 @@ int launch_gemm(const moe_problem& p, int mode, const void* a_act, const float* 
                 const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out,
                 float* out_scales, int32_t* err, void* ws, cudaStream_t st);
 size_t gemm_workspace_bytes(const moe_problem& p);
+int launch_grouped_ffn(const moe_problem& p, const void* xg, const float* xg_scales, const void* w13,
+                       const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
+                       const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err, void* ws,
+                       cudaStream_t st);
 int launch_eplb_record(const moe_problem& p, const int32_t* masked_m, int64_t pass, int window, int32_t* load_window,
                        cudaStream_t st);
 int launch_eplb_rebalance(const moe_problem& p, const int32_t* load_window, int window, const int32_t* p2l,
@@ -128,6 +132,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
   }
   return true;
+}
+
+// ---- flags between CTAs ----
+
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(int* p, int v) {
+  asm volatile("red.release.gpu.global.add.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Orders this thread's later async-proxy (TMA) reads of global memory after what it has acquired.
+__device__ __forceinline__ void fence_proxy_async_global() {
+  asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
 // ---- cp.async (asynchronous global -> shared copies) ----

@@ -47,6 +47,7 @@
 namespace moe {
 namespace {
 
+constexpr int MODE_FFN = 2;         // gate/up then down in one launch (units of both phases)
 constexpr int BM = 128;             // rows of one weight tile
 constexpr int BN = 128;             // token rows of one chunk at most
 constexpr int ROW_BYTES = 128;      // K bytes per stage row (one 128-byte swizzle span)
@@ -75,8 +76,9 @@ constexpr uint32_t TMEM_COLS = 512;  // two accumulator buffers of 256 columns
 // Bound of every wait: 4e9 SM cycles, about 2 s at the 2.07 GHz maximum clock.
 constexpr long long TIMEOUT = 4000000000LL;
 
-struct TcParams {
-  int nslots, masked, M_max;
+// One grouped GEMM of the layer (gate/up + SwiGLU, or down).
+struct Phase {
+  int mode;          // MODE_SWIGLU or MODE_DOWN
   int kb_total;      // 128-byte K blocks of the reduction
   int kb_per_split;  // K blocks per split
   int ksplit;
@@ -86,18 +88,25 @@ struct TcParams {
   int a1_off;        // row of the second tile of a pair relative to the first
   int out_cols;      // columns of the output rows
   int scale_cols;    // K / 128 (e4m3 scales per row of weights and activations)
-  uint32_t a_tile_tx;  // bytes one 128-row weight tile adds to its stage's transaction count
-  uint32_t w_fmt;      // kind::f8f6f4 format of the weight operand (0 = e4m3, 5 = e2m1)
-  int stages;
-  const int32_t* masked_m;
-  const int32_t* offsets;
   const float* a_scales;  // weight block scales [slots * NA/128][K/128]
   const float* b_scales;  // activation group scales [rows][K/128]
   void* out;
   float* out_scales;      // e4m3 gate/up output scales [rows][I/128]
   float* part;            // split-K partial sums [ksplit][rows_total][out_cols] fp32
-  long rows_total;        // rows of the grouped buffers
+};
+
+struct TcParams {
+  int nslots, masked, M_max;
+  uint32_t a_tile_tx;  // bytes one 128-row weight tile adds to its stage's transaction count
+  uint32_t w_fmt;      // kind::f8f6f4 format of the weight operand (0 = e4m3, 5 = e2m1)
+  int stages;
+  int nphase;          // 1, or 2 when gate/up and down run in one launch
+  const int32_t* masked_m;
+  const int32_t* offsets;
+  long rows_total;     // rows of the grouped buffers
   int32_t* err;
+  int* ready;          // two-phase launch: gate/up units finished per slot
+  Phase ph[2];
   uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
 };
 
@@ -116,8 +125,7 @@ __device__ __forceinline__ int slot_rows(const TcParams& p, int s) {
   return max(m, 0);
 }
 
-template <int MODE>
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* prefix, int u) {
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, int mode, const int* prefix, int u) {
   int lo = 0, hi = p.nslots;  // prefix[lo] <= u < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -131,18 +139,18 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const int* prefix
   const int r = u - prefix[lo];
   const int m = slot_rows(p, lo);
   const int nch = (m + BN - 1) / BN;
-  U.q = r % p.ksplit;
-  const int rest = r / p.ksplit;
+  U.q = r % f.ksplit;
+  const int rest = r / f.ksplit;
   U.c = rest % nch;
   U.j = rest / nch;
   const int base = m / nch, extra = m - base * nch;  // near-equal chunks
   U.nvalid = base + (U.c < extra ? 1 : 0);
   U.rowB = (p.masked ? lo * p.M_max : __ldg(p.offsets + lo)) + U.c * base + min(U.c, extra);
-  U.rowA0 = lo * p.NA + U.j * p.pair_stride;
-  U.rowA1 = U.rowA0 + p.a1_off;
-  U.a1 = (MODE == MODE_SWIGLU) ? true : (U.j * p.pair_stride + p.a1_off < p.NA);
-  U.kb0 = U.q * p.kb_per_split;
-  U.kb1 = min(p.kb_total, U.kb0 + p.kb_per_split);
+  U.rowA0 = lo * f.NA + U.j * f.pair_stride;
+  U.rowA1 = U.rowA0 + f.a1_off;
+  U.a1 = (mode == MODE_SWIGLU) ? true : (U.j * f.pair_stride + f.a1_off < f.NA);
+  U.kb0 = U.q * f.kb_per_split;
+  U.kb1 = min(f.kb_total, U.kb0 + f.kb_per_split);
   return U;
 }
 
@@ -161,14 +169,18 @@ template <bool F8, int MODE, bool TM>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
                            const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
-                           const __grid_constant__ CUtensorMap tmB128, const TcParams p) {
+                           const __grid_constant__ CUtensorMap tmB128, const __grid_constant__ CUtensorMap tmA2,
+                           const __grid_constant__ CUtensorMap tmC16, const __grid_constant__ CUtensorMap tmC32,
+                           const __grid_constant__ CUtensorMap tmC64, const __grid_constant__ CUtensorMap tmC128,
+                           const TcParams p) {
+  // tmA / tmB*: weights and token boxes of phase 0; tmA2 / tmC*: those of phase 1 (MODE_FFN)
   static_assert(TM || !F8, "FP8 / FP4 run token-major");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [RING][BN] activation scales of one K block
   float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [RING][2 tiles] weight scales of one K block
   float* red = reinterpret_cast<float*>(smem + p.red_off);  // [2 parities][512] group maxima
-  int* prefix = reinterpret_cast<int*>(smem + p.pre_off);   // [nslots + 1] unit prefix
+  int* prefix = reinterpret_cast<int*>(smem + p.pre_off);   // [nphase][nslots + 1] unit prefix
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* tfull = empty + p.stages;  // [2] accumulator buffer written
@@ -205,32 +217,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tmem_alloc(tmem_base_smem, TMEM_COLS);
     tmem_relinquish();
   }
-  // unit counts per slot -> prefix
+  // unit counts per slot -> prefix (one list per phase; the units of phase 1 follow phase 0's)
+  constexpr int NPH = (MODE == MODE_FFN) ? 2 : 1;
+  const int pstride = p.nslots + 1;
   for (int s = tid; s < p.nslots; s += NUM_THREADS) {
     const int nch = (slot_rows(p, s) + BN - 1) / BN;
-    prefix[s + 1] = nch * p.pairs * p.ksplit;
+#pragma unroll
+    for (int h = 0; h < NPH; ++h) prefix[h * pstride + s + 1] = nch * p.ph[h].pairs * p.ph[h].ksplit;
   }
-  if (tid == 0) prefix[0] = 0;
+  if (tid == 0) {
+#pragma unroll
+    for (int h = 0; h < NPH; ++h) prefix[h * pstride] = 0;
+  }
   tc_fence_before_sync();
   __syncthreads();
-  if (warp == 0) {
+  if (warp < NPH) {
+    int* pre = prefix + warp * pstride;
     int run = 0;
     for (int base = 1; base <= p.nslots; base += 32) {
       const int i = base + lane;
-      int v = (i <= p.nslots) ? prefix[i] : 0;
+      int v = (i <= p.nslots) ? pre[i] : 0;
 #pragma unroll
       for (int off = 1; off < 32; off <<= 1) {
         const int n = __shfl_up_sync(0xffffffffu, v, off);
         if (lane >= off) v += n;
       }
-      if (i <= p.nslots) prefix[i] = run + v;
+      if (i <= p.nslots) pre[i] = run + v;
       run += __shfl_sync(0xffffffffu, v, 31);
     }
   }
   __syncthreads();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_base_smem;
-  const int total = prefix[p.nslots];
+  const int total0 = prefix[p.nslots];
+  const int total = (MODE == MODE_FFN) ? total0 + prefix[pstride + p.nslots] : total0;
+  // Two-phase launch: a down unit reads rows of h (and their scales) that gate/up units of
+  // other CTAs wrote; wait (bounded) until every gate/up unit of slot s has released them.
+  auto wait_ready = [&](int s) -> bool {
+    const int m = slot_rows(p, s);
+    const int need = ((m + BN - 1) / BN) * p.ph[0].pairs * p.ph[0].ksplit * EPI_WARPS;  // one release per epilogue warp
+    const long long t0 = clock64();
+    while (ld_acquire_gpu(p.ready + s) < need) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > TIMEOUT) {
+        *abort_flag = 1;
+        return false;
+      }
+      __nanosleep(64);
+    }
+    fence_proxy_async_global();
+    return true;
+  };
+  // unit u -> (phase, its GEMM mode, the unit of that phase)
+  auto locate = [&](int u, int& h, int& mode) -> Unit {
+    h = (MODE == MODE_FFN && u >= total0) ? 1 : 0;
+    mode = (MODE == MODE_FFN) ? p.ph[h].mode : MODE;
+    return decode_unit(p, p.ph[h], mode, prefix + h * pstride, h ? u - total0 : u);
+  };
 
   if (warp < EPI_WARP0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(Regs<F8>::ctrl));
@@ -244,28 +287,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tma_prefetch_map(&tmB32);
           tma_prefetch_map(&tmB64);
         }
+        if (MODE == MODE_FFN) {
+          tma_prefetch_map(&tmA2);
+          tma_prefetch_map(&tmC128);
+        }
         const uint64_t pol = policy_evict_first();
         const int kb_elems = F8 ? ROW_BYTES : ROW_BYTES / 2;
         int stage = 0;
         uint32_t phase = 0;
         long issued = 0;
         bool ok = true;
+        // Two-phase launch: a down unit's first stage requests its weight tiles first and its
+        // token tile (rows of h) only once the slot's gate/up units have released them.
         for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
-          const Unit U = decode_unit<MODE>(p, prefix, u);
-          const CUtensorMap* mb = &tmB128;
+          int h, mode;
+          const Unit U = locate(u, h, mode);
+          const CUtensorMap* ma = h ? &tmA2 : &tmA;
+          const CUtensorMap* mb = h ? &tmC128 : &tmB128;
           int box = 128;
           if (!TM) {
             if (U.nvalid <= 16) {
-              mb = &tmB16;
+              mb = h ? &tmC16 : &tmB16;
               box = 16;
             } else if (U.nvalid <= 32) {
-              mb = &tmB32;
+              mb = h ? &tmC32 : &tmB32;
               box = 32;
             } else if (U.nvalid <= 64) {
-              mb = &tmB64;
+              mb = h ? &tmC64 : &tmB64;
               box = 64;
             }
           }
+          bool check_ready = (MODE == MODE_FFN) && h == 1;
           const uint32_t bytes = p.a_tile_tx * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
           for (int kb = U.kb0; kb < U.kb1; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT)) {
@@ -275,14 +327,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint8_t* st = smem + (size_t)stage * STAGE_BYTES;
             mbar_arrive_expect_tx(&full[stage], bytes);
             const int x = kb * kb_elems;
-            tma_load_2d_hint(st, &tmA, &full[stage], x, U.rowA0, pol);
-            if (U.a1) tma_load_2d_hint(st + TILE_A_BYTES, &tmA, &full[stage], x, U.rowA1, pol);
+            tma_load_2d_hint(st, ma, &full[stage], x, U.rowA0, pol);
+            if (U.a1) tma_load_2d_hint(st + TILE_A_BYTES, ma, &full[stage], x, U.rowA1, pol);
+            if (check_ready) {
+              check_ready = false;
+              if (!wait_ready(U.s)) ok = false;  // the stage is still completed below, then the loop ends
+            }
             tma_load_2d(st + 2 * TILE_A_BYTES, mb, &full[stage], x, U.rowB);
             ++issued;
             if (++stage == p.stages) {
               stage = 0;
               phase ^= 1u;
             }
+            if (!ok) break;
           }
         }
         if (!ok) {
@@ -306,7 +363,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         bool any = false;
         for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
-          const Unit U = decode_unit<MODE>(p, prefix, u);
+          int h, mode;
+          const Unit U = locate(u, h, mode);
           // weight-major: M = 128 weight rows, N = tokens rounded to 16 (one MMA per tile);
           // token-major: M = 128 token rows, N = both weight tiles (one MMA)
           // (token-major: the weights are the B operand, of format w_fmt)
@@ -385,8 +443,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t g = 0;  // K blocks staged so far
       bool ok = true;
       for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
-        const Unit U = decode_unit<MODE>(p, prefix, u);
+        int h, mode;
+        const Unit U = locate(u, h, mode);
+        const Phase& f = p.ph[h];
         const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
+        bool check_ready = (MODE == MODE_FFN) && h == 1;  // h scales of a down unit: written by gate/up units
         for (int k0 = U.kb0; ok && k0 < U.kb1; k0 += SG) {
           const int nk = min(SG, U.kb1 - k0);
           for (int j = 0; j < nk; ++j) {
@@ -397,17 +458,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           if (!ok) break;
+          if (check_ready) {
+            check_ready = false;
+            if (!wait_ready(U.s)) {
+              ok = false;
+              break;
+            }
+          }
           // activation scales of the chunk's rows: element (c, j) = b_scales[rowB + c][k0 + j]
           const int n = U.nvalid * nk;
           for (int idx = lt; idx < n; idx += LOAD_THREADS) {
             const int c = idx / nk, j = idx - c * nk;
-            cp_async4(sx + ((g + j) % RING) * BN + c, p.b_scales + (size_t)(U.rowB + c) * p.scale_cols + k0 + j);
+            cp_async4(sx + ((g + j) % RING) * BN + c, f.b_scales + (size_t)(U.rowB + c) * f.scale_cols + k0 + j);
           }
           // weight block scales of the two tiles (a missing second tile's value is never used)
           for (int idx = lt; idx < 2 * nk; idx += LOAD_THREADS) {
             const int j = idx >> 1, t = idx & 1;
             if (t == 0 || U.a1)
-              cp_async4(sw + ((g + j) % RING) * 2 + t, p.a_scales + (size_t)(t ? ra1 : ra0) * p.scale_cols + k0 + j);
+              cp_async4(sw + ((g + j) % RING) * 2 + t, f.a_scales + (size_t)(t ? ra1 : ra0) * f.scale_cols + k0 + j);
           }
           for (int j = 0; j < nk; ++j) cp_async_arrive_noinc(&rfull[(g + j) % RING]);
           g += nk;
@@ -425,11 +493,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc_it = 0, r_it = 0, u_it = 0;
     uint32_t ephase = 0;
     bool ok = true;
-    const size_t oc = (size_t)p.out_cols;
     // one arrival per warp, after the warp's own threads are ordered by __syncwarp
     auto warp_arrive = [&](uint64_t* bar) {
       __syncwarp();
       if (lane == 0) mbar_arrive(bar);
+    };
+    // Two-phase launch: each epilogue warp releases its rows of a finished gate/up unit later,
+    // once the stores have long landed (after the next unit's K loop, or before a down unit,
+    // which may itself be waiting for them); the down side counts EPI_WARPS releases per unit.
+    int pending = -1;
+    auto release_pending = [&]() {
+      if (MODE == MODE_FFN && pending >= 0) {
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) red_release_gpu_add(p.ready + pending, 1);
+        pending = -1;
+      }
     };
     // bounded barriers among the epilogue threads (a plain bar.sync could not give up)
     auto epi_sync = [&]() {
@@ -439,9 +518,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       return r;
     };
     for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++u_it) {
-      const Unit U = decode_unit<MODE>(p, prefix, u);
+      int h, mode;
+      const Unit U = locate(u, h, mode);
+      const Phase& f = p.ph[h];
+      const size_t oc = (size_t)f.out_cols;
       const int nkb = U.kb1 - U.kb0;
-      const bool split = p.ksplit > 1;
+      const bool split = f.ksplit > 1;
+      if (h == 1) release_pending();
       // weight-major: this thread owns weight row lrow of each tile and token columns
       // [c_lo, c_lo + ncols); token-major: token row lrow and weight columns [64*half, +64)
       const int c_lo = half * 64;
@@ -522,10 +605,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (split) {
         // this split's fp32 partial sums go to the dense [split][row][column] workspace; a
         // separate reduction kernel adds the splits in split order (no atomics, no waits)
-        float* pq = p.part + (size_t)U.q * p.rows_total * oc;
+        float* pq = f.part + (size_t)U.q * p.rows_total * oc;
         if constexpr (TM) {
           if (lrow < U.nvalid) {
-            float* prow = pq + (size_t)(U.rowB + lrow) * oc + (size_t)U.j * p.pair_stride + c_lo;
+            float* prow = pq + (size_t)(U.rowB + lrow) * oc + (size_t)U.j * f.pair_stride + c_lo;
 #pragma unroll
             for (int v = 0; v < 16; ++v) {
               reinterpret_cast<float4*>(prow)[v] =
@@ -536,7 +619,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         } else {
-          const size_t col0 = (size_t)U.j * p.pair_stride + lrow;
+          const size_t col0 = (size_t)U.j * f.pair_stride + lrow;
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             if (i < ncols) {
@@ -549,12 +632,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         continue;
       }
 
+      release_pending();
       // ---- final values of this unit
       float* redp = red + (size_t)(u_it & 1u) * 512;  // maxima, double-buffered by unit parity
       if constexpr (TM) {
         const bool row_ok = lrow < U.nvalid;
         const size_t row = (size_t)(U.rowB + lrow);
-        if constexpr (MODE == MODE_SWIGLU) {
+        if (mode == MODE_SWIGLU) {
           // rows past the chunk hold other tokens' data: no SwiGLU, no store
           if (row_ok) {
 #pragma unroll
@@ -574,7 +658,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float amax = fmaxf(redp[lrow], redp[128 + lrow]);
               const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
               const float inv = 1.0f / sc;  // one division per group; the codes use h * (1/s)
-              uint8_t* dst = static_cast<uint8_t*>(p.out) + row * oc + col;
+              uint8_t* dst = static_cast<uint8_t*>(f.out) + row * oc + col;
 #pragma unroll
               for (int v = 0; v < 4; ++v) {
                 const float* h = acc0 + 16 * v;
@@ -585,11 +669,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 w.w = pack_e4m3x4(h[12] * inv, h[13] * inv, h[14] * inv, h[15] * inv);
                 reinterpret_cast<uint4*>(dst)[v] = w;
               }
-              if (half == 0) p.out_scales[row * (oc / 128) + U.j] = sc;
+              if (half == 0) f.out_scales[row * (oc / 128) + U.j] = sc;
             }
           } else {
             if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(p.out) + row * oc + col);
+              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.out) + row * oc + col);
 #pragma unroll
               for (int v = 0; v < 8; ++v)
                 dst[v] = make_uint4(pack_bf16x2(acc0[8 * v + 0], acc0[8 * v + 1]),
@@ -600,8 +684,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         } else {
           if (row_ok) {
-            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(p.out) + row * oc;
-            uint4* d0 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * p.pair_stride + c_lo);
+            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(f.out) + row * oc;
+            uint4* d0 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * f.pair_stride + c_lo);
 #pragma unroll
             for (int v = 0; v < 8; ++v)
               d0[v] = make_uint4(pack_bf16x2(acc0[8 * v + 0], acc0[8 * v + 1]),
@@ -609,7 +693,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                  pack_bf16x2(acc0[8 * v + 4], acc0[8 * v + 5]),
                                  pack_bf16x2(acc0[8 * v + 6], acc0[8 * v + 7]));
             if (U.a1) {
-              uint4* d1 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * p.pair_stride + BM + c_lo);
+              uint4* d1 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * f.pair_stride + BM + c_lo);
 #pragma unroll
               for (int v = 0; v < 8; ++v)
                 d1[v] = make_uint4(pack_bf16x2(acc1[8 * v + 0], acc1[8 * v + 1]),
@@ -621,14 +705,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       } else {
         // weight-major: this thread holds output column (weight row) col0 for token columns c_lo + i
-        const int col0 = (MODE == MODE_SWIGLU) ? U.j * BM + lrow : U.j * p.pair_stride + lrow;
+        const int col0 = (mode == MODE_SWIGLU) ? U.j * BM + lrow : U.j * f.pair_stride + lrow;
         {
-          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(p.out);
+          __nv_bfloat16* o = static_cast<__nv_bfloat16*>(f.out);
 #pragma unroll
           for (int i = 0; i < 64; ++i) {
             if (i < ncols) {
               const size_t row = (size_t)(U.rowB + c_lo + i);
-              if constexpr (MODE == MODE_SWIGLU) {
+              if (mode == MODE_SWIGLU) {
                 o[row * oc + col0] = __float2bfloat16_rn(silu(acc0[i]) * acc1[i]);
               } else {
                 o[row * oc + col0] = __float2bfloat16_rn(acc0[i]);
@@ -638,7 +722,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
       }
+      if (MODE == MODE_FFN && mode == MODE_SWIGLU) pending = U.s;  // released later (see release_pending)
     }
+    release_pending();
   }
 
   tc_fence_before_sync();
@@ -691,7 +777,7 @@ struct Plan {
   size_t part_bytes;
 };
 
-Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
+Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int nphase = 1) {
   Plan pl{};
   const bool f8 = fp8_acts(p);
   const int esz = f8 ? 1 : 2;
@@ -751,7 +837,7 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   const size_t sx_b = f8 ? (size_t)RING * BN * 4 : 0;
   const size_t sw_b = f8 ? (size_t)RING * 2 * 4 : 0;
   const size_t red_b = (size_t)2 * 512 * 4;
-  const size_t pre_b = (size_t)(pl.nslots + 1) * 4;
+  const size_t pre_b = (size_t)nphase * (pl.nslots + 1) * 4;
   pl.stages = 0;
   for (int st = 6; st >= 2; --st) {
     extra = (size_t)st * STAGE_BYTES;
@@ -772,32 +858,37 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap) {
   return pl;
 }
 
+// Register split and shared-memory limit of one kernel instantiation, checked once per device
+// (the flags are per instantiation: all of them share one function type).
 template <bool F8, int MODE, bool TM>
-int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float* act_scales, const void* w,
-              const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
-              int32_t* err, void* ws, cudaStream_t st) {
-  const DeviceInfo& di = device_info();
+int prepare_kernel() {
+  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM>;
+  const int needed_regs = Regs<F8>::needed;
   static bool attr_set[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM>;
-  if (dev < 64 && !attr_set[dev]) {
-    // the register split above must fit in what the launch provides, or setmaxnreg.inc would wait forever
-    cudaFuncAttributes fa{};
-    if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return MOE_ERR_CUDA;
-    if (fa.numRegs * NUM_THREADS < Regs<F8>::needed) return MOE_ERR_UNSUPPORTED;
-    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, di.max_smem_optin) != cudaSuccess)
-      return MOE_ERR_CUDA;
-    attr_set[dev] = true;
-  }
-  const int esz = F8 ? 1 : 2;
-  const CUtensorMapDataType dt = F8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-  const int K = (MODE == MODE_SWIGLU) ? p.H : p.I;
-  const int NA = (MODE == MODE_SWIGLU) ? 2 * p.I : p.H;
-  const uint64_t rowsA = (uint64_t)pl.nslots * NA;
+  if (dev < 64 && attr_set[dev]) return MOE_OK;
+  // the register split must fit in what the launch provides, or setmaxnreg.inc would wait forever
+  cudaFuncAttributes fa{};
+  if (cudaFuncGetAttributes(&fa, kern) != cudaSuccess) return MOE_ERR_CUDA;
+  if (fa.numRegs * NUM_THREADS < needed_regs) return MOE_ERR_UNSUPPORTED;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, device_info().max_smem_optin) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  if (dev < 64) attr_set[dev] = true;
+  return MOE_OK;
+}
+
+// Tensor maps of one GEMM: the weights (tA) and the grouped activations in 16/32/64/128-row boxes.
+int make_maps(const moe_problem& p, int mode, const void* act, const void* w, CUtensorMap& tA, CUtensorMap* tB) {
+  const bool f8 = fp8_acts(p);
+  const int esz = f8 ? 1 : 2;
+  const CUtensorMapDataType dt = f8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  const int K = (mode == MODE_SWIGLU) ? p.H : p.I;
+  const int NA = (mode == MODE_SWIGLU) ? 2 * p.I : p.H;
+  const uint64_t rowsA = (uint64_t)(p.P + p.has_shared) * NA;
   const uint64_t rowsB = (uint64_t)grouped_rows(p);
   const uint32_t box_k = ROW_BYTES / esz;
-  CUtensorMap tA, tB[4];
   // e2m1 weights: packed 4-bit rows of K/2 bytes; TMA spreads each 8 bytes of codes over
   // 16 bytes of shared memory (the layout kind::f8f6f4 reads) and counts the 8 bytes read
   const bool w4 = p.wt == MOE_E2M1;
@@ -808,29 +899,45 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   for (int i = 0; i < 4; ++i)
     if (encode_tensor_map(&tB[i], dt, K, rowsB, (uint64_t)K * esz, box_k, boxes[i], act) != CUDA_SUCCESS)
       return MOE_ERR_CUDA;
+  return MOE_OK;
+}
 
+Phase make_phase(const moe_problem& p, int mode, const Plan& pl, const float* act_scales, const float* w_scales,
+                 void* out, float* out_scales, float* part) {
+  Phase f{};
+  const int K = (mode == MODE_SWIGLU) ? p.H : p.I;
+  f.mode = mode;
+  f.kb_total = pl.kb_total;
+  f.kb_per_split = pl.kb_per_split;
+  f.ksplit = pl.ksplit;
+  f.NA = (mode == MODE_SWIGLU) ? 2 * p.I : p.H;
+  f.pairs = pl.pairs;
+  f.pair_stride = (mode == MODE_SWIGLU) ? BM : 2 * BM;
+  f.a1_off = (mode == MODE_SWIGLU) ? p.I : BM;
+  f.out_cols = (mode == MODE_SWIGLU) ? p.I : p.H;
+  f.scale_cols = K / 128;
+  f.a_scales = w_scales;
+  f.b_scales = act_scales;
+  f.out = out;
+  f.out_scales = out_scales;
+  f.part = pl.ksplit > 1 ? part : nullptr;
+  return f;
+}
+
+TcParams make_params(const moe_problem& p, const Plan& pl, const int32_t* masked_m, const int32_t* offsets,
+                     int32_t* err) {
   TcParams prm{};
   prm.nslots = pl.nslots;
   prm.masked = p.layout == MOE_LAYOUT_MASKED;
   prm.M_max = p.M_max;
-  prm.kb_total = pl.kb_total;
-  prm.kb_per_split = pl.kb_per_split;
-  prm.ksplit = pl.ksplit;
-  prm.NA = NA;
-  prm.pairs = pl.pairs;
-  prm.pair_stride = (MODE == MODE_SWIGLU) ? BM : 2 * BM;
-  prm.a1_off = (MODE == MODE_SWIGLU) ? p.I : BM;
-  prm.out_cols = (MODE == MODE_SWIGLU) ? p.I : p.H;
-  prm.scale_cols = K / 128;
+  const bool w4 = p.wt == MOE_E2M1;
   prm.a_tile_tx = w4 ? TILE_A_BYTES / 2 : TILE_A_BYTES;
   prm.w_fmt = w4 ? 5u : 0u;
   prm.stages = pl.stages;
+  prm.nphase = 1;
   prm.masked_m = masked_m;
   prm.offsets = offsets;
-  prm.a_scales = w_scales;
-  prm.b_scales = act_scales;
-  prm.out = out;
-  prm.out_scales = out_scales;
+  prm.rows_total = (long)grouped_rows(p);
   prm.err = err;
   prm.sx_off = pl.sx_off;
   prm.sw_off = pl.sw_off;
@@ -838,17 +945,74 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   prm.pre_off = pl.pre_off;
   prm.bar_off = pl.bar_off;
   prm.misc_off = pl.misc_off;
-  prm.rows_total = (long)rowsB;
-  if (pl.ksplit > 1) prm.part = static_cast<float*>(ws);
-  kern<<<di.sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], prm);
+  return prm;
+}
+
+int launch_reduce(const moe_problem& p, const Plan& pl, const Phase& f, const int32_t* masked_m,
+                  const int32_t* offsets, cudaStream_t st) {
+  if (pl.ksplit <= 1) return MOE_OK;
+  const long rows = (long)grouped_rows(p);
+  splitk_reduce_kernel<<<(unsigned)rows, 256, 0, st>>>(f.part, pl.ksplit, rows, f.out_cols, masked_m, offsets,
+                                                       pl.nslots, p.layout == MOE_LAYOUT_MASKED, p.M_max,
+                                                       static_cast<__nv_bfloat16*>(f.out));
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+template <bool F8, int MODE, bool TM>
+int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float* act_scales, const void* w,
+              const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
+              int32_t* err, void* ws, cudaStream_t st) {
+  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM>;
+  int r = prepare_kernel<F8, MODE, TM>();
+  if (r) return r;
+  CUtensorMap tA, tB[4];
+  r = make_maps(p, MODE, act, w, tA, tB);
+  if (r) return r;
+  TcParams prm = make_params(p, pl, masked_m, offsets, err);
+  prm.ph[0] = make_phase(p, MODE, pl, act_scales, w_scales, out, out_scales, static_cast<float*>(ws));
+  prm.ph[1] = prm.ph[0];
+  kern<<<device_info().sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], tA, tB[0], tB[1],
+                                                             tB[2], tB[3], prm);
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  if (pl.ksplit > 1) {
-    splitk_reduce_kernel<<<(unsigned)rowsB, 256, 0, st>>>(prm.part, pl.ksplit, (long)rowsB, prm.out_cols, masked_m,
-                                                          offsets, pl.nslots, prm.masked, p.M_max,
-                                                          static_cast<__nv_bfloat16*>(out));
-    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  }
-  return MOE_OK;
+  return launch_reduce(p, pl, prm.ph[0], masked_m, offsets, st);
+}
+
+// Gate/up and down in one cooperative launch: every CTA works through the gate/up units and
+// then the down units; a down unit waits (bounded) until all gate/up units of its slot have
+// written their rows of h, so the down GEMM starts while the last gate/up units finish.
+template <bool F8, bool TM>
+int launch_ffn(const moe_problem& p, const Plan& pl0, const Plan& pl1, const void* xg, const float* xg_scales,
+               const void* w13, const float* w13_scales, const void* w2, const float* w2_scales,
+               const int32_t* masked_m, const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err,
+               void* ws, cudaStream_t st) {
+  auto kern = grouped_gemm_tc_kernel<F8, MODE_FFN, TM>;
+  int r = prepare_kernel<F8, MODE_FFN, TM>();
+  if (r) return r;
+  CUtensorMap tA, tB[4], tA2, tC[4];
+  if ((r = make_maps(p, MODE_SWIGLU, xg, w13, tA, tB))) return r;
+  if ((r = make_maps(p, MODE_DOWN, hg, w2, tA2, tC))) return r;
+  TcParams prm = make_params(p, pl0, masked_m, offsets, err);
+  prm.nphase = 2;
+  float* part = static_cast<float*>(ws);
+  prm.ph[0] = make_phase(p, MODE_SWIGLU, pl0, xg_scales, w13_scales, hg, hg_scales, nullptr);
+  prm.ph[1] = make_phase(p, MODE_DOWN, pl1, hg_scales, w2_scales, yg, nullptr, part);
+  prm.ready = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + align_up(pl1.part_bytes, 256));
+  if (cudaMemsetAsync(prm.ready, 0, sizeof(int) * pl0.nslots, st) != cudaSuccess) return MOE_ERR_CUDA;
+  // all CTAs must be resident at once (a down unit may wait for another CTA's gate/up unit)
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(device_info().sm_count);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = pl0.smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, tA, tB[0], tB[1], tB[2], tB[3], tA2, tC[0], tC[1], tC[2], tC[3], prm) !=
+      cudaSuccess)
+    return MOE_ERR_CUDA;
+  return launch_reduce(p, pl1, prm.ph[1], masked_m, offsets, st);
 }
 
 // ---------------------------------------------------------------------------
@@ -918,7 +1082,8 @@ size_t gemm_workspace_bytes(const moe_problem& p) {
       best = std::max(best, pl.part_bytes);
     }
   }
-  return best;
+  // the two-phase launch keeps one counter per slot after the split-K partial sums
+  return align_up(best, 256) + align_up(sizeof(int) * (size_t)(p.P + p.has_shared), 256);
 }
 
 int launch_gemm(const moe_problem& p, int mode, const void* act, const float* act_scales, const void* w,
@@ -960,6 +1125,29 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
   if (pl.tm) MOE_LAUNCH(false, MODE_DOWN, true);
   MOE_LAUNCH(false, MODE_DOWN, false);
 #undef MOE_LAUNCH
+}
+
+int launch_grouped_ffn(const moe_problem& p, const void* xg, const float* xg_scales, const void* w13,
+                       const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
+                       const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err, void* ws,
+                       cudaStream_t st) {
+  if (p.wt == MOE_F32) {  // CUDA-core path: the two GEMMs one after the other
+    int r = launch_gemm(p, MODE_SWIGLU, xg, nullptr, w13, nullptr, masked_m, offsets, hg, nullptr, err, ws, st);
+    if (r) return r;
+    return launch_gemm(p, MODE_DOWN, hg, nullptr, w2, nullptr, masked_m, offsets, yg, nullptr, err, ws, st);
+  }
+  const DeviceInfo& di = device_info();
+  const Plan pl0 = make_plan(p, MODE_SWIGLU, di.sm_count, di.max_smem_optin, 2);
+  const Plan pl1 = make_plan(p, MODE_DOWN, di.sm_count, di.max_smem_optin, 2);
+  if (pl0.stages == 0 || pl1.stages != pl0.stages || pl1.smem != pl0.smem) return MOE_ERR_UNSUPPORTED;
+  if (fp8_acts(p))
+    return launch_ffn<true, true>(p, pl0, pl1, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg,
+                                  hg_scales, yg, err, ws, st);
+  if (pl0.tm)
+    return launch_ffn<false, true>(p, pl0, pl1, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets,
+                                   hg, hg_scales, yg, err, ws, st);
+  return launch_ffn<false, false>(p, pl0, pl1, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg,
+                                  hg_scales, yg, err, ws, st);
 }
 
 }  // namespace moe

@@ -74,14 +74,23 @@ class MoeLayer:
         L.moe_grouped_down_gemm(self.p, self.hg, self.hg_s, self.w2, self.w2_s, self.masked_m, self.offsets,
                                 self.yg, self.err, self.ws, stream)
 
+    def ffn(self, stream=None):
+        """gate/up + SwiGLU and down in one launch (moe_grouped_ffn); same outputs as swiglu() + down()."""
+        L.moe_grouped_ffn(self.p, self.xg, self.xg_s, self.w13, self.w13_s, self.w2, self.w2_s, self.masked_m,
+                          self.offsets, self.hg, self.hg_s, self.yg, self.err, self.ws, stream)
+
     def combine(self, stream=None):
         L.moe_combine(self.p, self.yg, self.row_of, self.w, self.out, stream)
 
-    def forward(self, x, logits, stream=None):
-        """route -> permute -> gate/up -> down -> combine; returns self.out."""
+    def forward(self, x, logits, stream=None, fused=False):
+        """route -> permute -> gate/up -> down -> combine; returns self.out.  fused=True runs
+        gate/up and down as one launch (ffn())."""
         self.route(logits, stream)
         self.permute(x, stream)
-        self.swiglu(stream)
-        self.down(stream)
+        if fused:
+            self.ffn(stream)
+        else:
+            self.swiglu(stream)
+            self.down(stream)
         self.combine(stream)
         return self.out

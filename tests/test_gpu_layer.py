@@ -23,10 +23,10 @@ def built():
     build.build()
 
 
-def check_layer(wl, tokens=None):
+def check_layer(wl, tokens=None, fused=False):
     cfg = wl.cfg
     L = wl.layer()
-    out = L.forward(to_dev(wl.x), to_dev(wl.logits))
+    out = L.forward(to_dev(wl.x), to_dev(wl.logits), fused=fused)
     torch.cuda.synchronize()
     assert int(to_host(L.err)[0]) == 0
     assert (to_host(L.ids) == wl.ids).all()
@@ -43,15 +43,18 @@ def check_layer(wl, tokens=None):
     return L, lay
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("name", list(SMALL))
-def test_layer_small(name):
-    check_layer(Workload(SMALL[name]))
+def test_layer_small(name, fused):
+    check_layer(Workload(SMALL[name]), fused=fused)
 
 
+@pytest.mark.parametrize("fused", [False, True])
 @pytest.mark.parametrize("T", [1, 2, 7])
-def test_layer_few_tokens(T):
-    check_layer(Workload(SMALL["e4m3_masked_shared"].replace(T=T, M_max=T)))
-    check_layer(Workload(SMALL["bf16_masked"].replace(T=T, M_max=T)))
+def test_layer_few_tokens(T, fused):
+    check_layer(Workload(SMALL["e4m3_masked_shared"].replace(T=T, M_max=T)), fused=fused)
+    check_layer(Workload(SMALL["bf16_masked"].replace(T=T, M_max=T)), fused=fused)
+    check_layer(Workload(SMALL["e2m1_masked_shared"].replace(T=T, M_max=T)), fused=fused)
 
 
 def test_layer_all_tokens_on_few_experts():
@@ -64,7 +67,8 @@ def test_layer_all_tokens_on_few_experts():
     assert (lay["masked_m"][cfg.K:cfg.P] == 0).all()
 
 
-def test_layer_empty_batch():
+@pytest.mark.parametrize("fused", [False, True])
+def test_layer_empty_batch(fused):
     cfg = SMALL["bf16_masked"].replace(T=0, M_max=4)
     wl = Workload(SMALL["bf16_masked"])
     wl.cfg = cfg
@@ -73,7 +77,7 @@ def test_layer_empty_batch():
     wl.ids = np.zeros((0, cfg.K), np.int32)
     L = wl.layer()
     L.forward(torch.empty((0, cfg.H), dtype=torch.bfloat16, device="cuda"),
-              torch.empty((0, cfg.E), dtype=torch.float32, device="cuda"))
+              torch.empty((0, cfg.E), dtype=torch.float32, device="cuda"), fused=fused)
     torch.cuda.synchronize()
     assert (to_host(L.masked_m) == 0).all() and (to_host(L.offsets) == 0).all()
 
@@ -102,7 +106,8 @@ def test_layer_full_size_sampled(name, request):
     rng = np.random.default_rng(1)
     n = min(cfg.T, 24)
     tokens = np.unique(np.concatenate([[0, cfg.T - 1], rng.choice(cfg.T, n, replace=False)])).astype(np.int32)
-    L, lay = check_layer(wl, tokens=tokens)
+    # the benchmark's launch configuration: gate/up and down in one launch for bf16 experts
+    L, lay = check_layer(wl, tokens=tokens, fused=(cfg.gemm == "bf16"))
     if cfg.gemm == "e4m3":
         # dispatch quantisation bit-exact on the sampled tokens' rows
         rows = lay["row_of"][tokens].ravel()

@@ -215,6 +215,45 @@ def test_grouped_down(workloads, name):
     assert (real(to_host(L.yg)[~valid], cfg.y_dtype) == -3.0).all()
 
 
+@pytest.mark.parametrize("name", NAMES)
+def test_grouped_ffn_one_launch(workloads, name):
+    """moe_grouped_ffn: gate/up and down in one launch.  yg within tolerance of the oracle's
+    two steps; hg, its scales and yg bit-identical to the two separate calls; padding rows
+    untouched."""
+    wl = workloads[name]
+    cfg = wl.cfg
+    lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
+    hg_ref, hgs_ref = oracle.grouped_swiglu(cfg, xg, xgs, w13, w13s, lay["masked_m"], lay["offsets"])
+    yg_ref = oracle.grouped_down(cfg, hg_ref, hgs_ref, w2, w2s, lay["masked_m"], lay["offsets"])
+
+    def run(fused):
+        L = wl.layer()
+        L.xg.copy_(to_dev(xg))
+        if xgs is not None:
+            L.xg_s.copy_(to_dev(xgs))
+        L.masked_m.copy_(to_dev(lay["masked_m"]))
+        L.offsets.copy_(to_dev(lay["offsets"]))
+        L.yg.fill_(-3.0)
+        if fused:
+            L.ffn()
+        else:
+            L.swiglu()
+            L.down()
+        torch.cuda.synchronize()
+        assert int(to_host(L.err)[0]) == 0
+        return to_host(L.hg), None if L.hg_s is None else to_host(L.hg_s), to_host(L.yg)
+
+    hs, hss, ys = run(False)
+    hf, hfs, yf = run(True)
+    valid = lay["src_of"] >= 0
+    assert (hf[valid] == hs[valid]).all()
+    if hss is not None:
+        assert (hfs[valid] == hss[valid]).all()
+    assert (yf[valid] == ys[valid]).all()
+    assert (real(yf[~valid], cfg.y_dtype) == -3.0).all()
+    assert rel_err(real(yf[valid], cfg.y_dtype), real(yg_ref[valid], cfg.y_dtype)) <= TOL[cfg.gemm]
+
+
 # ---- a5 combine ---------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", NAMES)
