@@ -75,79 +75,101 @@ void launch_route_per(const moe_problem& p, const float* logits, int32_t* ids, f
 // "MoE inference and expert parallelism", routing section, Table 3-1 (DeepSeek-V3):
 // sigmoid scores, e_score_correction_bias used for the choice only, grouped
 // top-k (the best topk_group of n_group contiguous expert groups, a group
-// scored by its best biased score, then the K best experts inside them).  The
-// keys are formed and compared in fp64 (ties to the lower index); weights are
-// the unbiased scores of the chosen experts, renormalised if asked, times
-// `scale`.  One CTA per token: its 128 threads evaluate the E fp64 sigmoids
-// (fp64 throughput is low, so they are spread over the whole CTA), then warp 0
-// makes the choices from shared memory.
-constexpr int GROUPED_THREADS = 128;
+// scored by its best biased score, then the K best experts inside them; ties to
+// the lower index); weights are the unbiased scores of the chosen experts,
+// renormalised if asked, times `scale`.
+//
+// The choice is defined on fp64 keys sigmoid(l) + bias.  GB300's fp64 rate is
+// low, so each token (one warp) first chooses on fp32 keys, whose error against
+// the fp64 keys is below 2^-20 (1 + |key|) (a few ulps of the fp32 sigmoid plus
+// the rounding of the sum).  Every decision the choice makes -- the last kept
+// group against the best dropped one, each chosen expert against the next in
+// the list, and the last chosen against the best one left -- compares two keys;
+// when all those gaps exceed 2^-16 (1 + |key|) the fp64 keys order the same way
+// and the fp32 choice is the fp64 choice.  Otherwise (near-ties, exact ties) the
+// token is chosen again on fp64 keys.  The weights are the fp32 sigmoids of the
+// chosen experts (expf and an IEEE division: a few ulps), summed in k order.
+template <typename KT>
+__device__ __forceinline__ KT key_lowest() {
+  if constexpr (sizeof(KT) == 8) return (KT)0;  // order images of fp64 keys (below every real key)
+  else return -INFINITY;
+}
 
-template <int PER>  // keys held per lane of warp 0: E <= 32 * PER
-__global__ void __launch_bounds__(GROUPED_THREADS) route_grouped_kernel(const float* __restrict__ logits,
-                                                                        const float* __restrict__ bias, int T, int E,
-                                                                        int K, int n_group, int topk_group,
-                                                                        int renorm, float scale,
-                                                                        int32_t* __restrict__ ids,
-                                                                        float* __restrict__ w) {
-  __shared__ double s_sc[1024], s_key[1024];
-  const int t = blockIdx.x;
-  const float* l = logits + (size_t)t * E;
-  for (int e = threadIdx.x; e < E; e += GROUPED_THREADS) {
-    const double sc = 1.0 / (1.0 + exp(-(double)__ldg(l + e)));
-    s_sc[e] = sc;
-    s_key[e] = sc + (bias ? (double)__ldg(bias + e) : 0.0);
-  }
-  __syncthreads();
-  if (threadIdx.x >= 32) return;
-  const int lane = threadIdx.x;
-  const int gs = E / n_group;
-  double key[PER];
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = lane + 32 * i;
-    key[i] = (e < E) ? s_key[e] : -INFINITY;
-  }
+// fp64 key of one expert, kept out of line: the fallback is rare and its code stays small.
+__device__ __noinline__ double key_fp64(const float* l, const float* bias, int e) {
+  return 1.0 / (1.0 + exp(-(double)__ldg(l + e))) + (bias ? (double)__ldg(bias + e) : 0.0);
+}
+
+// Order-preserving image of an fp64 key as an unsigned integer (larger key, larger image).
+__device__ __forceinline__ uint64_t order_image(double k) {
+  const uint64_t u = (uint64_t)__double_as_longlong(k);
+  return (u >> 63) ? ~u : (u | 0x8000000000000000ull);
+}
+
+// The grouped choice on one warp's keys (float keys, or order images of fp64 keys).
+// With float keys it also reports whether every decision had a decisive gap
+// (`clear`) and the lowest key a decision touched (`cut`).
+template <int PER, typename KT>
+__device__ __forceinline__ void grouped_choice(const KT (&key)[PER], int lane, int E, int gs, int n_group,
+                                               int topk_group, int K, int& my_id, bool& clear, KT& cut) {
+  constexpr bool F = sizeof(KT) == 4;
+  const KT NEG = key_lowest<KT>();
+  auto kmax = [](KT a, KT b) { return a > b ? a : b; };
+  auto gap_ok = [](KT a, KT b) {  // a is ordered before b: is the gap decisive?
+    if constexpr (F) return a - b > 0x1p-16f * (1.0f + fabsf(a));  // a - b is exact when the two are close
+    else return true;
+  };
   // group maxima: lane g keeps the score of group g
-  double gmine = -INFINITY;
+  KT gmine = NEG;
   for (int g = 0; g < n_group; ++g) {
-    double m = -INFINITY;
+    KT m = NEG;
     const int e_lo = g * gs, e_hi = e_lo + gs;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
       const int e = lane + 32 * i;
-      if (e >= e_lo && e < e_hi) m = fmax(m, key[i]);
+      if (e >= e_lo && e < e_hi) m = kmax(m, key[i]);
     }
 #pragma unroll
-    for (int off = 16; off > 0; off >>= 1) m = fmax(m, __shfl_xor_sync(0xffffffffu, m, off));
+    for (int off = 16; off > 0; off >>= 1) m = kmax(m, __shfl_xor_sync(0xffffffffu, m, off));
     if (lane == g) gmine = m;
   }
-  // the topk_group best groups (ties to the lower group index)
+  clear = true;
+  // the topk_group best groups (ties to the lower group index), then the best group left
   uint32_t gsel = 0;
-  for (int r = 0; r < topk_group; ++r) {
+  KT last = NEG;
+  for (int r = 0; r <= topk_group && r < n_group; ++r) {
     const bool cand = lane < n_group && !((gsel >> lane) & 1u);
-    double bv = cand ? gmine : -INFINITY;
+    KT bv = cand ? gmine : NEG;
     int bg = cand ? lane : 0x7fffffff;
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const KT ov = __shfl_xor_sync(0xffffffffu, bv, off);
       const int og = __shfl_xor_sync(0xffffffffu, bg, off);
       if (og != 0x7fffffff && (bg == 0x7fffffff || ov > bv || (ov == bv && og < bg))) {
         bv = ov;
         bg = og;
       }
     }
-    gsel |= 1u << bg;
+    if (r == topk_group) {  // the best dropped group
+      clear = clear && gap_ok(last, bv);
+    } else {
+      gsel |= 1u << bg;
+      last = bv;
+    }
   }
+  cut = last;
   uint32_t avail = 0;
 #pragma unroll
   for (int i = 0; i < PER; ++i) {
     const int e = lane + 32 * i;
     if (e < E && ((gsel >> (e / gs)) & 1u)) avail |= 1u << i;
   }
-  int my_id = 0;
-  for (int k = 0; k < K; ++k) {
-    double bv = -INFINITY;
+  // the K best experts of the kept groups in order, then the best one left
+  const int ncand = topk_group * gs;
+  my_id = 0;
+  last = NEG;
+  for (int k = 0; k <= K && k < ncand; ++k) {
+    KT bv = NEG;
     int be = 0x7fffffff;
 #pragma unroll
     for (int i = 0; i < PER; ++i) {
@@ -160,30 +182,73 @@ __global__ void __launch_bounds__(GROUPED_THREADS) route_grouped_kernel(const fl
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) {
-      const double ov = __shfl_xor_sync(0xffffffffu, bv, off);
+      const KT ov = __shfl_xor_sync(0xffffffffu, bv, off);
       const int oe = __shfl_xor_sync(0xffffffffu, be, off);
       if (oe != 0x7fffffff && (be == 0x7fffffff || ov > bv || (ov == bv && oe < be))) {
         bv = ov;
         be = oe;
       }
     }
+    if (k > 0) clear = clear && gap_ok(last, bv);
+    if (be != 0x7fffffff && bv < cut) cut = bv;
+    if (k == K) break;
+    last = bv;
     if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
     if (lane == k) my_id = be;
   }
-  const double my_sc = (lane < K) ? s_sc[my_id] : 0.0;
-  double sum = 0.0;
+}
+
+template <int PER>
+__global__ void __launch_bounds__(256) route_grouped_kernel(const float* __restrict__ logits,
+                                                            const float* __restrict__ bias, int T, int E, int K,
+                                                            int n_group, int topk_group, int renorm, float scale,
+                                                            int32_t* __restrict__ ids, float* __restrict__ w) {
+  const int lane = threadIdx.x & 31;
+  const int t = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
+  if (t >= T) return;
+  const float* l = logits + (size_t)t * E;
+  const int gs = E / n_group;
+  int my_id = 0;
+  bool clear = false;
+  float key[PER];
+#pragma unroll
+  for (int i = 0; i < PER; ++i) {
+    const int e = lane + 32 * i;
+    key[i] = -INFINITY;
+    if (e < E) key[i] = __fdividef(1.0f, 1.0f + __expf(-__ldg(l + e))) + (bias ? __ldg(bias + e) : 0.0f);
+  }
+  float cut;
+  grouped_choice<PER, float>(key, lane, E, gs, n_group, topk_group, K, my_id, clear, cut);
+  if (!clear) {
+    // A near-tie: choose on the fp64 keys.  Only keys at or above the lowest key a decision
+    // touched (less the fp32 error) can change a decision, so only those are evaluated in
+    // fp64; the choice then runs on their order images (integer compares, no fp64 pipe).
+    const float lim = cut - 0x1p-18f * (1.0f + fabsf(cut));
+    uint64_t k64[PER];
+#pragma unroll 1
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      k64[i] = (e < E && key[i] >= lim) ? order_image(key_fp64(l, bias, e)) : 0;
+    }
+    uint64_t cut64;
+    grouped_choice<PER, uint64_t>(k64, lane, E, gs, n_group, topk_group, K, my_id, clear, cut64);
+  }
+  const float my_sc = (lane < K) ? 1.0f / (1.0f + expf(-__ldg(l + my_id))) : 0.0f;
+  float sum = 0.0f;
   for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, my_sc, k);  // fixed order
   if (lane < K) {
     ids[(size_t)t * K + lane] = my_id;
-    w[(size_t)t * K + lane] = (float)((renorm ? my_sc / sum : my_sc) * (double)scale);
+    w[(size_t)t * K + lane] = (renorm ? my_sc / sum : my_sc) * scale;
   }
 }
 
 template <int PER>
 void launch_grouped_per(const moe_problem& p, const float* logits, const float* bias, int n_group, int topk_group,
                         int renorm, float scale, int32_t* ids, float* w, cudaStream_t st) {
-  route_grouped_kernel<PER><<<p.T, GROUPED_THREADS, 0, st>>>(logits, bias, p.T, p.E, p.K, n_group, topk_group,
-                                                             renorm, scale, ids, w);
+  const int threads = 256;
+  const int blocks = (int)(((int64_t)p.T * 32 + threads - 1) / threads);
+  route_grouped_kernel<PER><<<blocks, threads, 0, st>>>(logits, bias, p.T, p.E, p.K, n_group, topk_group, renorm,
+                                                        scale, ids, w);
 }
 
 }  // namespace
