@@ -37,7 +37,7 @@ METRIC = "MoE layer tokens/s"
 TRAFFIC = {
     # one-launch gate/up + down kernel, ncu --set full (profiles/gemm_ffn_mixtral_decode.md):
     # 2.821602 GB read + 5.709 MB written
-    "mixtral_decode:ffn:673cc1410b1c19a1": 2827311312,
+    "mixtral_decode:ffn:7a66cd5626512fe6": 2827311312,  # kernel code unchanged since (comments only)
 }
 
 

@@ -29,13 +29,18 @@
 //   * Warp 0: TMA producer (weights with an evict-first L2 hint).  Warp 1:
 //     tensor-memory allocator and the single MMA-issuing thread.  Warps 2-3:
 //     FP8 scale loaders (the activation and weight scales of each K block into
-//     an 8-slot ring in shared memory, ahead of the epilogue; keeping the
-//     scales out of the stages leaves room for four 48 KB stages).  Warps 4-11:
-//     epilogue, two warps per tensor-memory lane quarter.
+//     a 32-slot ring in shared memory with asynchronous 4-byte copies, up to 32
+//     K blocks ahead of the epilogue; keeping the scales out of the stages
+//     leaves room for four 48 KB stages).  Warps 4-11: epilogue, two warps per
+//     tensor-memory lane quarter.
 //   * FP8: the MMAs of one 128-K block write one of two tensor-memory buffers;
 //     the epilogue reads it, scales it and adds it into fp32 registers while
 //     the MMA fills the other.  BF16: the whole K range accumulates in tensor
 //     memory; the two buffers alternate between units.
+//   * MODE_FFN runs gate/up and down in one cooperative launch: the unit list
+//     is the gate/up units followed by the down units, and a down unit's token
+//     (h) tile and scales are read only after every gate/up unit of its slot
+//     has released its rows through a per-slot counter.
 //   * Every wait is bounded in time; on expiry the CTA sets an abort flag,
 //     drains its copies and MMAs, frees tensor memory, reports
 //     MOE_FLAG_TIMEOUT and returns.
