@@ -159,6 +159,28 @@ class ClockSampler:
                 "samples": len(sm), "source": self.source}
 
 
+# ---- the multi-rank pieces (one replica of the layer per GPU; no data-path collective) ----
+
+def replica_seed(rank: int) -> int:
+    """Each replica draws its own batch: the generator seed is the rank."""
+    return rank
+
+
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The slowest rank's value (the timed region is bracketed by barriers on every rank)."""
+    if world <= 1:
+        return x
+    import torch
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(world: int, tokens_per_step: int, steps: int, total_ms: float) -> float:
+    """Whole-job tokens/s: every rank processes its own batch each step, timed by the slowest."""
+    return world * tokens_per_step * steps / (total_ms * 1e-3)
+
+
 def problem_of(cfg, moe):
     return moe.Problem.make(T=cfg.T, H=cfg.H, I=cfg.I, E=cfg.E, K=cfg.K, P=cfg.P, M_max=cfg.M_max,
                             has_shared=cfg.S, act=cfg.act, wt=cfg.wt, out=cfg.out, layout=cfg.layout)
@@ -189,7 +211,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
 
     dev = torch.device("cuda", local_rank)
     torch.cuda.set_device(dev)
-    seed = rank  # each replica its own batch
+    seed = replica_seed(rank)
     x, logits = mi.activations(cfg, seed)
     w13, w13s = mi.expert_weights(cfg, "w13")
     w2, w2s = mi.expert_weights(cfg, "w2")
@@ -272,10 +294,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
         torch.distributed.barrier()
     total_ms = ev[0][0].elapsed_time(ev[K - 1][NP])
     part_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(NP)}
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world, dev)
 
     # ---- end to end through the host: pinned inputs in, output back, every step
     xh = torch.from_numpy(np.ascontiguousarray(x).view(np.int16) if x.dtype == np.uint16 else x)
@@ -300,10 +319,7 @@ def run_gpu(args, cfg, rank, world, local_rank):
         e1.record(stream)
     stream.synchronize()
     e2e_ms = e0.elapsed_time(e1)
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
     assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
 
     aux = aux_timings(moe, L, cfg, ld, stream, torch) if world == 1 else None
@@ -510,8 +526,8 @@ def main():
     if rank == 0:
         K = args.steps
         ms = res["total_ms"] / K
-        value = world * cfg.T * K / (res["total_ms"] * 1e-3)
-        e2e = world * cfg.T * K / (res["e2e_ms"] * 1e-3)
+        value = job_throughput(world, cfg.T, K, res["total_ms"])
+        e2e = job_throughput(world, cfg.T, K, res["e2e_ms"])
         moe_src = src_hash("gemm_tc.cu", "common.cuh")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,

@@ -320,9 +320,29 @@ def test_rerun_bitwise_identical(workloads, name):
     L = wl.layer()
     x, lg = to_dev(wl.x), to_dev(wl.logits)
     a = to_host(L.forward(x, lg).clone())
-    for _ in range(2):
-        b = to_host(L.forward(x, lg).clone())
+    for fused in (False, True, True):  # the one-launch FFN gives the same bits, run after run
+        b = to_host(L.forward(x, lg, fused=fused).clone())
         assert (a == b).all()
+
+
+def test_grouped_ffn_rejects_bad_arguments():
+    wl = Workload(SMALL["e2m1_masked_shared"])
+    L = wl.layer()
+    f = moe.moe_grouped_ffn
+    base = [L.p, L.xg, L.xg_s, L.w13, L.w13_s, L.w2, L.w2_s, L.masked_m, L.offsets, L.hg, L.hg_s, L.yg, L.err, L.ws]
+    for i in (2, 4, 6, 10):  # e4m3 activations / e2m1 weights need every scale array
+        args = list(base)
+        args[i] = None
+        with pytest.raises(moe.MoeError):
+            f(*args)
+    args = list(base)
+    args[5] = L.w2.view(-1)[16:]  # packed 4-bit weights must start on a 32-byte boundary
+    with pytest.raises(moe.MoeError):
+        f(*args)
+    args = list(base)
+    args[13] = L.ws[:8]  # workspace too small for the per-slot counters
+    with pytest.raises(moe.MoeError):
+        f(*args)
 
 
 # ---- DeepSeek-V3 routing: sigmoid scores, correction bias, grouped top-k ------------
