@@ -283,6 +283,13 @@ moe_status moe_eplb_rebalance(const moe_problem* p, const int32_t* load_window, 
                               const int32_t* phys_to_log, int64_t* logical_load, int32_t* new_phys_to_log,
                               int32_t* err_flag, moe_stream_t stream);
 
+/* Diagnostic, an addition of this library (the pages describe none): runs the
+ * bounded wait that every kernel here uses on an mbarrier that nothing
+ * completes, with a limit of `cycles` SM cycles (1 .. 4e9), so that the expiry
+ * path can be checked without a fault: the kernel ORs MOE_FLAG_TIMEOUT into
+ * *err_flag (device int32) and returns; the context stays usable. */
+moe_status moe_selftest_bounded_wait(int64_t cycles, int32_t* err_flag, moe_stream_t stream);
+
 /* Host helper ("vLLM EPLB", section 1.2): invert a physical_to_logical map.
  * All pointers are HOST pointers.  p2l [P] in, l2p [E][R] out (slots of each
  * logical expert in ascending order, padded with -1), rc [E] out.  Returns

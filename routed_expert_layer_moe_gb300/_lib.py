@@ -25,7 +25,7 @@ LAYOUTS = {"masked": MOE_LAYOUT_MASKED, "contig": MOE_LAYOUT_CONTIG}
 EXPORTS = ["moe_version", "moe_status_string", "moe_grouped_rows", "moe_workspace_bytes", "moe_check_problem",
            "moe_route_topk", "moe_route_grouped_topk", "moe_permute", "moe_permute_no_workspace",
            "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_grouped_ffn", "moe_combine",
-           "moe_eplb_record", "moe_eplb_rebalance", "moe_eplb_invert"]
+           "moe_eplb_record", "moe_eplb_rebalance", "moe_eplb_invert", "moe_selftest_bounded_wait"]
 
 
 class MoeError(RuntimeError):
@@ -91,6 +91,8 @@ def lib():
     L.moe_eplb_record.restype = i32
     L.moe_eplb_rebalance.argtypes = [pp, vp, i32, vp, vp, vp, vp, vp]
     L.moe_eplb_rebalance.restype = i32
+    L.moe_selftest_bounded_wait.argtypes = [i64, vp, vp]
+    L.moe_selftest_bounded_wait.restype = i32
     L.moe_eplb_invert.argtypes = [i32, i32, vp, i32, vp, vp]
     L.moe_eplb_invert.restype = i32
     _lib = L
@@ -206,6 +208,10 @@ def moe_eplb_rebalance(p: Problem, load_window, window: int, phys_to_log, logica
     _check(lib().moe_eplb_rebalance(ctypes.byref(p), _ptr(load_window), int(window), _ptr(phys_to_log),
                                     _ptr(logical_load), _ptr(new_phys_to_log), _ptr(err_flag), _stream(stream)),
            "moe_eplb_rebalance")
+
+
+def moe_selftest_bounded_wait(cycles: int, err_flag, stream=None) -> None:
+    _check(lib().moe_selftest_bounded_wait(int(cycles), _ptr(err_flag), _stream(stream)), "moe_selftest_bounded_wait")
 
 
 def moe_eplb_invert(p2l, E: int, R: int):

@@ -269,6 +269,11 @@ moe_status moe_eplb_rebalance(const moe_problem* p, const int32_t* load_window, 
                                         err_flag, (cudaStream_t)stream));
 }
 
+moe_status moe_selftest_bounded_wait(int64_t cycles, int32_t* err_flag, moe_stream_t stream) {
+  if (!err_flag || cycles < 1 || cycles > 4000000000LL) return MOE_ERR_INVALID;
+  return launched(launch_bounded_wait_selftest((long long)cycles, err_flag, (cudaStream_t)stream));
+}
+
 int32_t moe_eplb_invert(int32_t P, int32_t E, const int32_t* p2l, int32_t R, int32_t* l2p, int32_t* rc) {
   if (P < 0 || E <= 0 || R <= 0 || !p2l || !l2p || !rc) return MOE_ERR_INVALID;
   for (int e = 0; e < E; ++e) {

@@ -47,6 +47,7 @@ int launch_eplb_record(const moe_problem& p, const int32_t* masked_m, int64_t pa
                        cudaStream_t st);
 int launch_eplb_rebalance(const moe_problem& p, const int32_t* load_window, int window, const int32_t* p2l,
                           int64_t* logical_load, int32_t* new_p2l, int32_t* err, cudaStream_t st);
+int launch_bounded_wait_selftest(long long cycles, int32_t* err, cudaStream_t st);
 int launch_combine(const moe_problem& p, const void* yg, const int32_t* row_of, const float* w, void* out,
                    cudaStream_t st);
 
@@ -132,6 +133,15 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
     }
   }
   return true;
+}
+
+// ---- wide stores ----
+
+// One 32-byte store (a full L2 sector); dst must be 32-byte aligned.
+__device__ __forceinline__ void st_global_v8(void* dst, uint4 a, uint4 b) {
+  asm volatile("st.global.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8};" ::"l"(dst), "r"(a.x), "r"(a.y), "r"(a.z),
+               "r"(a.w), "r"(b.x), "r"(b.y), "r"(b.z), "r"(b.w)
+               : "memory");
 }
 
 // ---- flags between CTAs ----

@@ -66,3 +66,30 @@ int launch_eplb_rebalance(const moe_problem& p, const int32_t* load_window, int 
 }
 
 }  // namespace moe
+
+// ---------------------------------------------------------------------------
+// Diagnostic: the bounded wait every kernel of the library uses, run to its limit.
+// ---------------------------------------------------------------------------
+namespace moe {
+namespace {
+
+// One thread waits on an mbarrier that nothing completes, with a bound of `cycles` SM
+// cycles; on expiry it reports MOE_FLAG_TIMEOUT as the layer kernels do, and returns.
+__global__ void bounded_wait_kernel(long long cycles, int32_t* err) {
+  __shared__ uint64_t bar;
+  __shared__ int abort_flag;
+  if (threadIdx.x != 0) return;
+  abort_flag = 0;
+  mbar_init(&bar, 1);
+  fence_barrier_init();
+  if (!mbar_wait(&bar, 0, &abort_flag, cycles)) atomicOr(err, MOE_FLAG_TIMEOUT);
+}
+
+}  // namespace
+
+int launch_bounded_wait_selftest(long long cycles, int32_t* err, cudaStream_t st) {
+  bounded_wait_kernel<<<1, 32, 0, st>>>(cycles, err);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

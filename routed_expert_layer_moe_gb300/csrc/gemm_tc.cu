@@ -66,7 +66,7 @@ constexpr int EPI_WARPS = EPI_THREADS / 32;  // epilogue barriers take one arriv
 constexpr int LOAD_WARP0 = 2;       // warps 2 and 3 load FP8 scales
 constexpr int LOAD_THREADS = 64;
 constexpr int RING = 32;            // K blocks of scales staged ahead of the epilogue
-constexpr int SG = 16;              // K blocks of scales fetched per loader pass
+constexpr int SG = 16;              // K blocks of scales fetched per loader pass (RING / 2: two groups in flight)
 // Register split (setmaxnreg): warpgroup 0 (TMA, MMA, scale loads) gives
 // registers to the two epilogue warpgroups, which hold 2 x 64 fp32
 // accumulators per thread.  4*32*ctrl + 8*32*epi must not exceed
@@ -130,7 +130,10 @@ __device__ __forceinline__ int slot_rows(const TcParams& p, int s) {
   return max(m, 0);
 }
 
-__device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, int mode, const int* prefix, int u) {
+// srows / sbase: each slot's valid rows and first grouped-buffer row, staged in shared memory
+// at kernel start (a unit's decode then needs no global load).
+__device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, int mode, const int* prefix,
+                                            const int* srows, const int* sbase, int u) {
   int lo = 0, hi = p.nslots;  // prefix[lo] <= u < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -142,7 +145,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
   Unit U;
   U.s = lo;
   const int r = u - prefix[lo];
-  const int m = slot_rows(p, lo);
+  const int m = srows[lo];
   const int nch = (m + BN - 1) / BN;
   U.q = r % f.ksplit;
   const int rest = r / f.ksplit;
@@ -150,7 +153,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
   U.j = rest / nch;
   const int base = m / nch, extra = m - base * nch;  // near-equal chunks
   U.nvalid = base + (U.c < extra ? 1 : 0);
-  U.rowB = (p.masked ? lo * p.M_max : __ldg(p.offsets + lo)) + U.c * base + min(U.c, extra);
+  U.rowB = sbase[lo] + U.c * base + min(U.c, extra);
   U.rowA0 = lo * f.NA + U.j * f.pair_stride;
   U.rowA1 = U.rowA0 + f.a1_off;
   U.a1 = (mode == MODE_SWIGLU) ? true : (U.j * f.pair_stride + f.a1_off < f.NA);
@@ -162,6 +165,37 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
   const __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
   return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// 64 consecutive values of one row as bf16 (128 bytes): 32-byte stores when the row is
+// 32-byte aligned (wide), else 16-byte ones.
+__device__ __forceinline__ void store_bf16x64(__nv_bfloat16* dst, const float* a, bool wide) {
+  auto pk = [&](int v) {
+    return make_uint4(pack_bf16x2(a[8 * v + 0], a[8 * v + 1]), pack_bf16x2(a[8 * v + 2], a[8 * v + 3]),
+                      pack_bf16x2(a[8 * v + 4], a[8 * v + 5]), pack_bf16x2(a[8 * v + 6], a[8 * v + 7]));
+  };
+  if (wide) {
+#pragma unroll
+    for (int v = 0; v < 4; ++v) st_global_v8(dst + 16 * v, pk(2 * v), pk(2 * v + 1));
+  } else {
+#pragma unroll
+    for (int v = 0; v < 8; ++v) reinterpret_cast<uint4*>(dst)[v] = pk(v);
+  }
+}
+
+// 64 consecutive fp32 values (256 bytes), same store widths.
+__device__ __forceinline__ void store_f32x64(float* dst, const float* a, bool wide) {
+  auto q = [&](int v) {
+    return make_uint4(__float_as_uint(a[4 * v]), __float_as_uint(a[4 * v + 1]), __float_as_uint(a[4 * v + 2]),
+                      __float_as_uint(a[4 * v + 3]));
+  };
+  if (wide) {
+#pragma unroll
+    for (int v = 0; v < 8; ++v) st_global_v8(dst + 8 * v, q(2 * v), q(2 * v + 1));
+  } else {
+#pragma unroll
+    for (int v = 0; v < 16; ++v) reinterpret_cast<uint4*>(dst)[v] = q(v);
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float d) {
@@ -186,6 +220,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   float* sw = reinterpret_cast<float*>(smem + p.sw_off);    // [RING][2 tiles] weight scales of one K block
   float* red = reinterpret_cast<float*>(smem + p.red_off);  // [2 parities][512] group maxima
   int* prefix = reinterpret_cast<int*>(smem + p.pre_off);   // [nphase][nslots + 1] unit prefix
+  int* srows = prefix + p.nphase * (p.nslots + 1);          // [nslots] valid rows per slot
+  int* sbase = srows + p.nslots;                            // [nslots] first grouped-buffer row per slot
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.stages;
   uint64_t* tfull = empty + p.stages;  // [2] accumulator buffer written
@@ -226,7 +262,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr int NPH = (MODE == MODE_FFN) ? 2 : 1;
   const int pstride = p.nslots + 1;
   for (int s = tid; s < p.nslots; s += NUM_THREADS) {
-    const int nch = (slot_rows(p, s) + BN - 1) / BN;
+    const int m = slot_rows(p, s);
+    srows[s] = m;
+    sbase[s] = p.masked ? s * p.M_max : __ldg(p.offsets + s);
+    const int nch = (m + BN - 1) / BN;
 #pragma unroll
     for (int h = 0; h < NPH; ++h) prefix[h * pstride + s + 1] = nch * p.ph[h].pairs * p.ph[h].ksplit;
   }
@@ -259,7 +298,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // Two-phase launch: a down unit reads rows of h (and their scales) that gate/up units of
   // other CTAs wrote; wait (bounded) until every gate/up unit of slot s has released them.
   auto wait_ready = [&](int s) -> bool {
-    const int m = slot_rows(p, s);
+    const int m = srows[s];
     const int need = ((m + BN - 1) / BN) * p.ph[0].pairs * p.ph[0].ksplit * EPI_WARPS;  // one release per epilogue warp
     const long long t0 = clock64();
     while (ld_acquire_gpu(p.ready + s) < need) {
@@ -277,7 +316,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto locate = [&](int u, int& h, int& mode) -> Unit {
     h = (MODE == MODE_FFN && u >= total0) ? 1 : 0;
     mode = (MODE == MODE_FFN) ? p.ph[h].mode : MODE;
-    return decode_unit(p, p.ph[h], mode, prefix + h * pstride, h ? u - total0 : u);
+    return decode_unit(p, p.ph[h], mode, prefix + h * pstride, srows, sbase, h ? u - total0 : u);
   };
 
   if (warp < EPI_WARP0) {
@@ -614,14 +653,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if constexpr (TM) {
           if (lrow < U.nvalid) {
             float* prow = pq + (size_t)(U.rowB + lrow) * oc + (size_t)U.j * f.pair_stride + c_lo;
-#pragma unroll
-            for (int v = 0; v < 16; ++v) {
-              reinterpret_cast<float4*>(prow)[v] =
-                  make_float4(acc0[4 * v], acc0[4 * v + 1], acc0[4 * v + 2], acc0[4 * v + 3]);
-              if (U.a1)
-                reinterpret_cast<float4*>(prow + BM)[v] =
-                    make_float4(acc1[4 * v], acc1[4 * v + 1], acc1[4 * v + 2], acc1[4 * v + 3]);
-            }
+            const bool wide = (reinterpret_cast<uintptr_t>(f.part) & 31u) == 0;  // offsets are 256-byte multiples
+            store_f32x64(prow, acc0, wide);
+            if (U.a1) store_f32x64(prow + BM, acc1, wide);
           }
         } else {
           const size_t col0 = (size_t)U.j * f.pair_stride + lrow;
@@ -664,48 +698,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const float sc = (amax == 0.0f) ? 1.0f : __fdiv_rn(amax, 448.0f);
               const float inv = 1.0f / sc;  // one division per group; the codes use h * (1/s)
               uint8_t* dst = static_cast<uint8_t*>(f.out) + row * oc + col;
-#pragma unroll
-              for (int v = 0; v < 4; ++v) {
+              auto pk = [&](int v) {
                 const float* h = acc0 + 16 * v;
-                uint4 w;
-                w.x = pack_e4m3x4(h[0] * inv, h[1] * inv, h[2] * inv, h[3] * inv);
-                w.y = pack_e4m3x4(h[4] * inv, h[5] * inv, h[6] * inv, h[7] * inv);
-                w.z = pack_e4m3x4(h[8] * inv, h[9] * inv, h[10] * inv, h[11] * inv);
-                w.w = pack_e4m3x4(h[12] * inv, h[13] * inv, h[14] * inv, h[15] * inv);
-                reinterpret_cast<uint4*>(dst)[v] = w;
+                return make_uint4(pack_e4m3x4(h[0] * inv, h[1] * inv, h[2] * inv, h[3] * inv),
+                                  pack_e4m3x4(h[4] * inv, h[5] * inv, h[6] * inv, h[7] * inv),
+                                  pack_e4m3x4(h[8] * inv, h[9] * inv, h[10] * inv, h[11] * inv),
+                                  pack_e4m3x4(h[12] * inv, h[13] * inv, h[14] * inv, h[15] * inv));
+              };
+              if ((reinterpret_cast<uintptr_t>(f.out) & 31u) == 0) {  // row and column offsets: 64-byte multiples
+                st_global_v8(dst, pk(0), pk(1));
+                st_global_v8(dst + 32, pk(2), pk(3));
+              } else {
+#pragma unroll
+                for (int v = 0; v < 4; ++v) reinterpret_cast<uint4*>(dst)[v] = pk(v);
               }
               if (half == 0) f.out_scales[row * (oc / 128) + U.j] = sc;
             }
           } else {
-            if (row_ok) {
-              uint4* dst = reinterpret_cast<uint4*>(static_cast<__nv_bfloat16*>(f.out) + row * oc + col);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                dst[v] = make_uint4(pack_bf16x2(acc0[8 * v + 0], acc0[8 * v + 1]),
-                                    pack_bf16x2(acc0[8 * v + 2], acc0[8 * v + 3]),
-                                    pack_bf16x2(acc0[8 * v + 4], acc0[8 * v + 5]),
-                                    pack_bf16x2(acc0[8 * v + 6], acc0[8 * v + 7]));
-            }
+            if (row_ok)
+              store_bf16x64(static_cast<__nv_bfloat16*>(f.out) + row * oc + col, acc0,
+                            (reinterpret_cast<uintptr_t>(f.out) & 31u) == 0);
           }
         } else {
           if (row_ok) {
-            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(f.out) + row * oc;
-            uint4* d0 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * f.pair_stride + c_lo);
-#pragma unroll
-            for (int v = 0; v < 8; ++v)
-              d0[v] = make_uint4(pack_bf16x2(acc0[8 * v + 0], acc0[8 * v + 1]),
-                                 pack_bf16x2(acc0[8 * v + 2], acc0[8 * v + 3]),
-                                 pack_bf16x2(acc0[8 * v + 4], acc0[8 * v + 5]),
-                                 pack_bf16x2(acc0[8 * v + 6], acc0[8 * v + 7]));
-            if (U.a1) {
-              uint4* d1 = reinterpret_cast<uint4*>(yrow + (size_t)U.j * f.pair_stride + BM + c_lo);
-#pragma unroll
-              for (int v = 0; v < 8; ++v)
-                d1[v] = make_uint4(pack_bf16x2(acc1[8 * v + 0], acc1[8 * v + 1]),
-                                   pack_bf16x2(acc1[8 * v + 2], acc1[8 * v + 3]),
-                                   pack_bf16x2(acc1[8 * v + 4], acc1[8 * v + 5]),
-                                   pack_bf16x2(acc1[8 * v + 6], acc1[8 * v + 7]));
-            }
+            __nv_bfloat16* yrow = static_cast<__nv_bfloat16*>(f.out) + row * oc + (size_t)U.j * f.pair_stride + c_lo;
+            const bool wide = (reinterpret_cast<uintptr_t>(f.out) & 31u) == 0;  // offsets are 128-byte multiples
+            store_bf16x64(yrow, acc0, wide);
+            if (U.a1) store_bf16x64(yrow + BM, acc1, wide);
           }
         }
       } else {
@@ -842,7 +861,7 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int n
   const size_t sx_b = f8 ? (size_t)RING * BN * 4 : 0;
   const size_t sw_b = f8 ? (size_t)RING * 2 * 4 : 0;
   const size_t red_b = (size_t)2 * 512 * 4;
-  const size_t pre_b = (size_t)nphase * (pl.nslots + 1) * 4;
+  const size_t pre_b = ((size_t)nphase * (pl.nslots + 1) + 2 * (size_t)pl.nslots) * 4;  // prefix, rows, bases
   pl.stages = 0;
   for (int st = 6; st >= 2; --st) {
     extra = (size_t)st * STAGE_BYTES;

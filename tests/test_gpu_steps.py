@@ -441,3 +441,19 @@ def test_eplb_rebalance_flags_and_rejects():
         moe.moe_eplb_rebalance(p2, window, W, bad, gl, gn, err)
     with pytest.raises(moe.MoeError):
         moe.moe_eplb_record(p, window, 0, 0, window)
+
+
+# ---- failure detection: a bounded wait that runs out --------------------------------
+
+def test_bounded_wait_expires_with_a_flag():
+    """The wait every kernel uses, on an mbarrier nothing completes: after its limit
+    (2e6 cycles, about a millisecond) the kernel reports MOE_FLAG_TIMEOUT and returns, and
+    the context keeps working."""
+    err = torch.zeros(1, dtype=torch.int32, device="cuda")
+    moe.moe_selftest_bounded_wait(2_000_000, err)
+    torch.cuda.synchronize()
+    assert int(to_host(err)[0]) == moe.MOE_FLAG_TIMEOUT
+    x = torch.arange(8, device="cuda", dtype=torch.float32)
+    assert float(x.sum().item()) == 28.0
+    with pytest.raises(moe.MoeError):
+        moe.moe_selftest_bounded_wait(0, err)
