@@ -128,6 +128,19 @@ int64_t moe_grouped_rows(const moe_problem* p);
  * ordered on one stream.  Returns 0 for an invalid problem. */
 size_t moe_workspace_bytes(const moe_problem* p);
 
+/* Issue counters ("Inference INFRA methodology (5)", section "DeepGEMM": a tile
+ * whose first row is at or past masked_m issues no MMA).  After a tensor-core
+ * moe_grouped_swiglu_gemm, moe_grouped_down_gemm or moe_grouped_ffn call, the
+ * first MOE_STATS_BYTES of the workspace hold int32 counters
+ * [2 phases][MOE_STATS_CTAS][2]: for each CTA, the units it issued (token
+ * chunk x weight-tile pair x K split) and the token tiles among them (one per
+ * slot and chunk of at most 128 rows).  Summed over CTAs, the token tiles of a
+ * GEMM equal the sum over slots of ceil(masked_m[s] / 128).  Phase 1 is the
+ * down GEMM of moe_grouped_ffn and zero otherwise.  The counters stay valid
+ * until the next call that uses the workspace. */
+#define MOE_STATS_CTAS 256
+#define MOE_STATS_BYTES (2 * MOE_STATS_CTAS * 2 * 4)
+
 /* Check a problem without touching the GPU: MOE_OK, MOE_ERR_INVALID or
  * MOE_ERR_UNSUPPORTED. */
 moe_status moe_check_problem(const moe_problem* p);

@@ -60,6 +60,10 @@ def _load():
     lib.orc_route.argtypes = [i32, i32, i32, vp, vp, vp]
     lib.orc_route_grouped.argtypes = [i32, i32, i32, vp, vp, i32, i32, i32, dbl, vp, vp]
     lib.orc_eplb_rebalance.argtypes = [i32, i32, i32, vp, vp, vp, vp]
+    lib.orc_token_tiles.argtypes = [i32, vp, i32]
+    lib.orc_token_tiles.restype = i64
+    lib.orc_pad_waste.argtypes = [i32, i32]
+    lib.orc_pad_waste.restype = dbl
     lib.orc_eplb_rebalance.restype = i32
     lib.orc_eplb_invert.argtypes = [i32, i32, vp, i32, vp, vp]
     lib.orc_eplb_invert.restype = i32
@@ -223,6 +227,17 @@ def eplb_rebalance(window, E: int, p2l=None):
     if r < 0:
         raise ValueError("invalid physical_to_logical map")
     return load, new
+
+
+def token_tiles(masked_m, BM: int = 128) -> int:
+    """Token tiles the grouped GEMMs issue: sum over slots of ceil(masked_m / BM)."""
+    mm = _c(masked_m, np.int32)
+    return int(_load().orc_token_tiles(mm.size, mm.ctypes.data, BM))
+
+
+def pad_waste(M_e: int, BM: int) -> float:
+    """MMA work over useful work for one expert of M_e rows in BM-row tiles."""
+    return float(_load().orc_pad_waste(M_e, BM))
 
 
 def layout(cfg, ids, p2l=None):

@@ -341,6 +341,20 @@ int orc_eplb_rebalance(int P, int E, int W, const int32_t* window, const int32_t
   return 0;
 }
 
+/* [INFRA-5] "DeepGEMM", the padding-waste example: an expert with M_e rows
+ * occupies ceil(M_e / BM) token tiles of BM rows, so the MMA work is
+ * ceil(M_e / BM) * BM / M_e times the useful work.  orc_token_tiles sums the
+ * tiles over the slots (a slot with no rows has none); orc_pad_waste is the
+ * ratio for one expert. */
+int64_t orc_token_tiles(int nslots, const int32_t* masked_m, int BM) {
+  int64_t n = 0;
+  for (int s = 0; s < nslots; ++s)
+    if (masked_m[s] > 0) n += (masked_m[s] + BM - 1) / BM;
+  return n;
+}
+
+double orc_pad_waste(int M_e, int BM) { return (double)((M_e + BM - 1) / BM) * BM / (double)M_e; }
+
 /* ------------------------------------------------------------------------ */
 /* a2: dispatch layout                                                       */
 /* ------------------------------------------------------------------------ */

@@ -17,6 +17,8 @@ MOE_OK, MOE_ERR_INVALID, MOE_ERR_UNSUPPORTED, MOE_ERR_CUDA, MOE_ERR_WORKSPACE = 
 MOE_F32, MOE_BF16, MOE_E4M3, MOE_E2M1 = 0, 1, 2, 3
 MOE_LAYOUT_MASKED, MOE_LAYOUT_CONTIG = 0, 1
 MOE_FLAG_OVERFLOW, MOE_FLAG_BAD_EXPERT, MOE_FLAG_BAD_MAP, MOE_FLAG_TIMEOUT = 1, 2, 4, 8
+MOE_STATS_CTAS = 256                        # issue counters at the start of the workspace (include/moe.h)
+MOE_STATS_BYTES = 2 * MOE_STATS_CTAS * 2 * 4
 
 DTYPES = {"f32": MOE_F32, "bf16": MOE_BF16, "e4m3": MOE_E4M3, "e2m1": MOE_E2M1}
 LAYOUTS = {"masked": MOE_LAYOUT_MASKED, "contig": MOE_LAYOUT_CONTIG}

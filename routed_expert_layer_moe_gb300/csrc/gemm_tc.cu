@@ -53,6 +53,8 @@ namespace moe {
 namespace {
 
 constexpr int MODE_FFN = 2;         // gate/up then down in one launch (units of both phases)
+constexpr int STATS_CTAS = 256;     // per-CTA issue counters kept at the start of the workspace
+constexpr size_t STATS_BYTES = 2 * STATS_CTAS * 2 * sizeof(int);
 constexpr int BM = 128;             // rows of one weight tile
 constexpr int BN = 128;             // token rows of one chunk at most
 constexpr int ROW_BYTES = 128;      // K bytes per stage row (one 128-byte swizzle span)
@@ -111,6 +113,7 @@ struct TcParams {
   long rows_total;     // rows of the grouped buffers
   int32_t* err;
   int* ready;          // two-phase launch: gate/up units finished per slot
+  int* stats;          // [2 phases][STATS_CTAS][2]: units and token tiles each CTA issued
   Phase ph[2];
   uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
 };
@@ -406,9 +409,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         uint32_t acc_it = 0;
         bool ok = true;
         bool any = false;
+        int units[2] = {0, 0}, tiles[2] = {0, 0};
         for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
           int h, mode;
           const Unit U = locate(u, h, mode);
+          ++units[h];
+          tiles[h] += (U.j == 0 && U.q == 0);  // one unit per (slot, token chunk) has j = q = 0
           // weight-major: M = 128 weight rows, N = tokens rounded to 16 (one MMA per tile);
           // token-major: M = 128 token rows, N = both weight tiles (one MMA)
           // (token-major: the weights are the B operand, of format w_fmt)
@@ -467,6 +473,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               tc_commit(&tfull[b]);
               ++acc_it;
             }
+          }
+        }
+        // issue counters of this launch (no tile exists for padding rows: token tiles per GEMM =
+        // sum over slots of ceil(rows / 128)); CTA 0 also clears the entries of absent CTAs
+        if (p.stats) {
+          for (int h = 0; h < 2; ++h) {
+            if (blockIdx.x < STATS_CTAS) {
+              p.stats[(h * STATS_CTAS + blockIdx.x) * 2] = units[h];
+              p.stats[(h * STATS_CTAS + blockIdx.x) * 2 + 1] = tiles[h];
+            }
+            if (blockIdx.x == 0)
+              for (int c = gridDim.x; c < STATS_CTAS; ++c) {
+                p.stats[(h * STATS_CTAS + c) * 2] = 0;
+                p.stats[(h * STATS_CTAS + c) * 2 + 1] = 0;
+              }
           }
         }
         if (!ok && any) {
@@ -993,7 +1014,9 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   r = make_maps(p, MODE, act, w, tA, tB);
   if (r) return r;
   TcParams prm = make_params(p, pl, masked_m, offsets, err);
-  prm.ph[0] = make_phase(p, MODE, pl, act_scales, w_scales, out, out_scales, static_cast<float*>(ws));
+  prm.stats = static_cast<int*>(ws);
+  prm.ph[0] = make_phase(p, MODE, pl, act_scales, w_scales, out, out_scales,
+                         reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + STATS_BYTES));
   prm.ph[1] = prm.ph[0];
   kern<<<device_info().sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], tA, tB[0], tB[1],
                                                              tB[2], tB[3], prm);
@@ -1017,10 +1040,11 @@ int launch_ffn(const moe_problem& p, const Plan& pl0, const Plan& pl1, const voi
   if ((r = make_maps(p, MODE_DOWN, hg, w2, tA2, tC))) return r;
   TcParams prm = make_params(p, pl0, masked_m, offsets, err);
   prm.nphase = 2;
-  float* part = static_cast<float*>(ws);
+  prm.stats = static_cast<int*>(ws);
+  float* part = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + STATS_BYTES);
   prm.ph[0] = make_phase(p, MODE_SWIGLU, pl0, xg_scales, w13_scales, hg, hg_scales, nullptr);
   prm.ph[1] = make_phase(p, MODE_DOWN, pl1, hg_scales, w2_scales, yg, nullptr, part);
-  prm.ready = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + align_up(pl1.part_bytes, 256));
+  prm.ready = reinterpret_cast<int*>(static_cast<uint8_t*>(ws) + STATS_BYTES + align_up(pl1.part_bytes, 256));
   if (cudaMemsetAsync(prm.ready, 0, sizeof(int) * pl0.nslots, st) != cudaSuccess) return MOE_ERR_CUDA;
   // all CTAs must be resident at once (a down unit may wait for another CTA's gate/up unit)
   cudaLaunchConfig_t cfg{};
@@ -1106,8 +1130,8 @@ size_t gemm_workspace_bytes(const moe_problem& p) {
       best = std::max(best, pl.part_bytes);
     }
   }
-  // the two-phase launch keeps one counter per slot after the split-K partial sums
-  return align_up(best, 256) + align_up(sizeof(int) * (size_t)(p.P + p.has_shared), 256);
+  // issue counters first, then the split-K partial sums, then (two-phase launch) one counter per slot
+  return STATS_BYTES + align_up(best, 256) + align_up(sizeof(int) * (size_t)(p.P + p.has_shared), 256);
 }
 
 int launch_gemm(const moe_problem& p, int mode, const void* act, const float* act_scales, const void* w,

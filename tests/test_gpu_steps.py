@@ -254,6 +254,37 @@ def test_grouped_ffn_one_launch(workloads, name):
     assert rel_err(real(yf[valid], cfg.y_dtype), real(yg_ref[valid], cfg.y_dtype)) <= TOL[cfg.gemm]
 
 
+@pytest.mark.parametrize("name", [n for n in NAMES if SMALL[n].gemm != "f32"])
+def test_gemm_issue_counters(workloads, name):
+    """The GEMMs' token tiles (summed over CTAs from the counters in the workspace) equal the
+    oracle's sum over slots of ceil(masked_m / 128): no tile for padding rows or empty slots;
+    every unit belongs to one such tile (units = tiles x tile pairs x K splits)."""
+    wl = workloads[name]
+    cfg = wl.cfg
+    lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
+    want = oracle.token_tiles(lay["masked_m"], 128)
+    L = wl.layer()
+    L.xg.copy_(to_dev(xg))
+    if xgs is not None:
+        L.xg_s.copy_(to_dev(xgs))
+    L.masked_m.copy_(to_dev(lay["masked_m"]))
+    L.offsets.copy_(to_dev(lay["offsets"]))
+
+    def counters():
+        torch.cuda.synchronize()
+        c = L.ws[:moe.MOE_STATS_BYTES].view(torch.int32).cpu().numpy().reshape(2, moe.MOE_STATS_CTAS, 2)
+        return c.sum(axis=1)  # [phase][units, tiles]
+
+    for call in (L.swiglu, L.down):
+        call()
+        c = counters()
+        assert c[0, 1] == want and c[1].sum() == 0
+        assert c[0, 0] % max(want, 1) == 0 and c[0, 0] >= want
+    L.ffn()
+    c = counters()
+    assert c[0, 1] == want and c[1, 1] == want
+
+
 # ---- a5 combine ---------------------------------------------------------------------
 
 @pytest.mark.parametrize("name", NAMES)

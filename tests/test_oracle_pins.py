@@ -33,6 +33,17 @@ def test_eplb_worked_example():
         assert r == max(case["logical_replica_count"])
 
 
+def test_pad_waste_worked_example():
+    """The pages' padding-waste figures at M_e = 5 rows (golden file), and the tile count they
+    rest on: ceil(rows / BM) tiles per slot with rows, none for an empty slot."""
+    g = json.load(open(os.path.join(GOLDEN, "deepgemm_pad_waste.json")))
+    for c in g["cases"]:
+        assert oracle.pad_waste(g["M_e"], c["BM"]) == pytest.approx(c["waste"], rel=1e-12)
+    mm = np.array([5, 0, 128, 129, 1, 256], np.int32)
+    assert oracle.token_tiles(mm, 128) == 1 + 0 + 1 + 2 + 1 + 2
+    assert oracle.token_tiles(mm, 16) == 1 + 0 + 8 + 9 + 1 + 16
+
+
 def test_eplb_rejects_bad_map():
     with pytest.raises(ValueError):
         oracle.eplb_invert([0, 1, 4], 4)
