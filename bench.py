@@ -429,6 +429,29 @@ def ffn_roofline(cfg, res, peaks, moe_src, split):
             "algorithmic_bytes": int(algo), "avg_launch_us": round(dur_s * 1e6, 2), "peak_source": src}
 
 
+def tensor_roofline(cfg, res, peaks, split):
+    """The dominant kernel against the dense tensor-core peak of its MMA type (the second
+    fraction the prefill workload reports): useful FLOPs (2 per multiply-add over the valid
+    rows) / its event-timed duration.  bf16: the measured sustained bf16 peak (the kernel runs
+    inside a long step); e4m3 and e2m1 x e4m3 (kind::f8f6f4, the FP8 rate): 2 x that, the
+    recipe's nominal FP8 / bf16 ratio."""
+    _, _, bf16_sus, src = peaks
+    rows = int(res["masked_m"].sum())
+    f13 = 2.0 * rows * 2 * cfg.I * cfg.H
+    f2 = 2.0 * rows * cfg.H * cfg.I
+    if split:
+        flops, dur = f13, res["part_ms"]["gate_up"] * 1e-3
+    else:
+        flops, dur = f13 + f2, res["part_ms"]["gate_up+down"] * 1e-3
+    if cfg.gemm == "f32":
+        return None
+    peak = bf16_sus * (2.0 if cfg.gemm == "e4m3" else 1.0)
+    ach = flops / dur / 1e12
+    return {"bound": "tensor", "achieved": round(ach, 1), "peak": round(peak, 1), "unit": "TFLOP/s",
+            "frac": round(ach / peak, 4), "flops": int(flops),
+            "peak_source": "%s (bf16 sustained%s)" % (src, " x 2 for FP8" if cfg.gemm == "e4m3" else "")}
+
+
 def cpu_baseline(cfg, x, logits, budget_s=12.0):
     """The oracle on the host cores, whole-layer tokens/s on a bounded sample of tokens."""
     import oracle
@@ -536,6 +559,7 @@ def main():
             "data": "synthetic (seeded generator, random-init experts)",
             "config": dict(config_dict(cfg, world), ffn="two launches" if args.split_ffn else "one launch"),
             "roofline": ffn_roofline(cfg, res, peaks, moe_src, args.split_ffn),
+            "roofline_tensor": tensor_roofline(cfg, res, peaks, args.split_ffn),
             "step_breakdown_us": {k: round(v * 1e3, 2) for k, v in res["part_ms"].items()},
             "touched_slots": res["touched"],
             "aux_calls_us": res["aux"],
