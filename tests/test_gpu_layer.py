@@ -57,6 +57,17 @@ def test_layer_few_tokens(T, fused):
     check_layer(Workload(SMALL["e2m1_masked_shared"].replace(T=T, M_max=T)), fused=fused)
 
 
+@pytest.mark.parametrize("fused", [False, True])
+@pytest.mark.parametrize("base,E,K", [("e4m3_masked_shared", 1023, 32), ("bf16_masked", 1024, 8),
+                                      ("e2m1_masked_shared", 1023, 16)])
+def test_layer_maximum_slots_and_k(base, E, K, fused):
+    """The largest problem the ABI takes in slots and experts per token: P + S = 1024 slots
+    (1023 routed experts + the shared one, or 1024 routed) and K up to 32, at small H and I;
+    every token checked."""
+    cfg = SMALL[base].replace(T=24, H=256, I=128, E=E, K=K, M_max=24)
+    check_layer(Workload(cfg), fused=fused)
+
+
 def test_layer_all_tokens_on_few_experts():
     cfg = SMALL["e4m3_masked_shared"]
     x, logits = mi.activations(cfg)
