@@ -135,6 +135,23 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volati
   return true;
 }
 
+// ---- packed fp32 arithmetic ----
+
+// (a0, a1) += (x0, x1) * s as one packed fp32x2 multiply-add: the same two roundings as two
+// fmaf calls, in one instruction.
+__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float s) {
+  asm("{\n"
+      "  .reg .b64 d, x, sv, c;\n"
+      "  mov.b64 x, {%2, %3};\n"
+      "  mov.b64 sv, {%4, %4};\n"
+      "  mov.b64 c, {%0, %1};\n"
+      "  fma.rn.f32x2 d, x, sv, c;\n"
+      "  mov.b64 {%0, %1}, d;\n"
+      "}\n"
+      : "+f"(a0), "+f"(a1)
+      : "f"(x0), "f"(x1), "f"(s));
+}
+
 // ---- wide stores ----
 
 // One 32-byte store (a full L2 sector); dst must be 32-byte aligned.

@@ -630,9 +630,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 warp_arrive(&tempty[b]);
               }
 #pragma unroll
-              for (int i = 0; i < 32; ++i) {
-                acc0[pr * 32 + i] = fmaf(v0[i], p0, acc0[pr * 32 + i]);
-                acc1[pr * 32 + i] = fmaf(v1[i], p1, acc1[pr * 32 + i]);
+              for (int i = 0; i < 32; i += 2) {
+                fma2(acc0[pr * 32 + i], acc0[pr * 32 + i + 1], v0[i], v0[i + 1], p0);
+                fma2(acc1[pr * 32 + i], acc1[pr * 32 + i + 1], v1[i], v1[i + 1], p1);
               }
             }
           }
