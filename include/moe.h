@@ -207,9 +207,9 @@ moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, 
  * fixed 4 MiB array inside the library, which every GPU that loads the library
  * keeps until the process exits.
  *   - A problem whose scratch exceeds 4 MiB is rejected with MOE_ERR_WORKSPACE
- *     before anything is enqueued (the scratch is 8*P*ceil(T/32) + 4*T*K +
- *     4*E*(P-E+2) bytes, each term rounded up to 256; the prefill workload
- *     T=8192, E=P=512, K=10 needs about 1.3 MiB).
+ *     before anything is enqueued (the scratch is (4*P*ceil(T/32) + 4) +
+ *     4*P*ceil(T/32) + 4*T*K + 4*E*(P-E+1) + 4*E bytes, each term rounded up
+ *     to 256; the prefill workload T=8192, E=P=512, K=10 needs about 1.3 MiB).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call outside of any
  *     stream capture.

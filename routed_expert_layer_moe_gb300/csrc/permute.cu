@@ -24,7 +24,7 @@ namespace moe {
 namespace {
 
 struct PermuteWs {
-  uint32_t* bits;   // [P][W]
+  uint32_t* bits;   // [P][W], then one int32 counter (cleared with the bits)
   int32_t* prefix;  // [P][W] rank of the first token of each 32-token word
   int32_t* slot_of; // [T*K]
   int32_t* l2p;     // [E][R]
@@ -44,7 +44,7 @@ PermuteWs carve(const moe_problem& p, void* ws, size_t* total) {
     off = align_up(off + bytes, 256);
     return ptr;
   };
-  w.bits = (uint32_t*)take((size_t)p.P * W * 4);
+  w.bits = (uint32_t*)take((size_t)p.P * W * 4 + 4);
   w.prefix = (int32_t*)take((size_t)p.P * W * 4);
   w.slot_of = (int32_t*)take((size_t)p.T * p.K * 4);
   w.l2p = (int32_t*)take((size_t)p.E * max_replicas(p) * 4);
@@ -165,6 +165,70 @@ __global__ void __launch_bounds__(1024) scan_kernel(const uint32_t* __restrict__
   if (threadIdx.x == blockDim.x - 1) offsets[NS] = excl + a + b;  // the total
 }
 
+// The same outputs for large bitmasks, spread over the GPU: a warp per slot (8 slots per
+// CTA) writes the slot's word prefixes and its count; the last CTA to finish (a counter in
+// the workspace, cleared with the bits) turns the counts into offsets.
+__global__ void __launch_bounds__(256) slot_scan_kernel(const uint32_t* __restrict__ bits, int W, int P, int S, int T,
+                                                        int masked, int M_max, int32_t* __restrict__ prefix,
+                                                        int32_t* masked_m, int32_t* __restrict__ offsets,
+                                                        int32_t* err, int* done) {
+  __shared__ int32_t warp_tot[8];
+  __shared__ int last;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int s = blockIdx.x * 8 + warp;
+  if (s < P) {
+    int base = 0;
+    for (int w0 = 0; w0 < W; w0 += 32) {
+      const int w = w0 + lane;
+      const int c = (w < W) ? __popc(bits[(size_t)s * W + w]) : 0;
+      int inc = c;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int n = __shfl_up_sync(0xffffffffu, inc, off);
+        if (lane >= off) inc += n;
+      }
+      if (w < W) prefix[(size_t)s * W + w] = base + inc - c;
+      base += __shfl_sync(0xffffffffu, inc, 31);
+    }
+    if (lane == 0) {
+      masked_m[s] = base;
+      if (masked && base > M_max) atomicOr(err, MOE_FLAG_OVERFLOW);
+    }
+  }
+  __threadfence();  // this CTA's counts are visible before it is counted as done
+  __syncthreads();
+  if (threadIdx.x == 0) last = (atomicAdd(done, 1) == (int)gridDim.x - 1);
+  __syncthreads();
+  if (!last) return;
+  __threadfence();
+  // exclusive scan of the counts (the shared slot holds T) into offsets, 256 threads in order
+  const int NS = P + S;
+  const int per = (NS + 255) / 256;
+  const int lo = threadIdx.x * per, hi = min(lo + per, NS);
+  int sum = 0;
+  for (int i = lo; i < hi; ++i) sum += (i < P) ? __ldcg(masked_m + i) : T;
+  int inc = sum;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int n = __shfl_up_sync(0xffffffffu, inc, off);
+    if (lane >= off) inc += n;
+  }
+  if (lane == 31) warp_tot[warp] = inc;
+  __syncthreads();
+  int before = 0;
+  for (int w = 0; w < warp; ++w) before += warp_tot[w];
+  int run = before + inc - sum;
+  for (int i = lo; i < hi; ++i) {
+    offsets[i] = run;
+    run += (i < P) ? __ldcg(masked_m + i) : T;
+  }
+  if (threadIdx.x == 255) offsets[NS] = before + inc;
+  if (S && threadIdx.x == 0) {
+    masked_m[P] = T;
+    if (masked && T > M_max) atomicOr(err, MOE_FLAG_OVERFLOW);
+  }
+}
+
 // One CTA per token.
 template <typename TX, bool QUANT>
 __global__ void __launch_bounds__(256) scatter_kernel(const TX* __restrict__ x, int H, int T, int K, int P, int S,
@@ -273,7 +337,7 @@ int launch_permute(const moe_problem& p, const int32_t* ids, const void* x, cons
   const int masked = p.layout == MOE_LAYOUT_MASKED;
   const int R = max_replicas(p);
   if (p.P > 0 && W > 0) {
-    if (cudaMemsetAsync(w.bits, 0, (size_t)p.P * W * 4, st) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaMemsetAsync(w.bits, 0, (size_t)p.P * W * 4 + 4, st) != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (p2l) eplb_tables_kernel<<<1, 1024, 0, st>>>(p2l, p.P, p.E, R, w.l2p, w.rc, err);
   if (p.T > 0) {
@@ -281,8 +345,13 @@ int launch_permute(const moe_problem& p, const int32_t* ids, const void* x, cons
     mark_kernel<<<(n + 255) / 256, 256, 0, st>>>(ids, p.T, p.K, p.E, p2l != nullptr, w.l2p, w.rc, R, w.bits, W,
                                                  w.slot_of, err);
   }
-  scan_kernel<<<1, 1024, 0, st>>>(w.bits, W, p.P, p.has_shared, p.T, masked, p.M_max, w.prefix, masked_m, offsets,
-                                  err);
+  if ((size_t)p.P * W >= 8192) {  // large bitmask (prefill): a warp per slot across the GPU
+    slot_scan_kernel<<<(p.P + 7) / 8, 256, 0, st>>>(w.bits, W, p.P, p.has_shared, p.T, masked, p.M_max, w.prefix,
+                                                    masked_m, offsets, err, reinterpret_cast<int*>(w.bits + (size_t)p.P * W));
+  } else {
+    scan_kernel<<<1, 1024, 0, st>>>(w.bits, W, p.P, p.has_shared, p.T, masked, p.M_max, w.prefix, masked_m, offsets,
+                                    err);
+  }
   if (p.T > 0) {
     if (fp8_acts(p)) {
       scatter_kernel<__nv_bfloat16, true><<<p.T, 256, 0, st>>>(

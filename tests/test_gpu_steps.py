@@ -110,6 +110,23 @@ def test_permute(workloads, name):
         assert (real(gx[~valid], cfg.gemm) == -3.0).all()
 
 
+@pytest.mark.parametrize("base,shared", [("e4m3_contig", 0), ("e4m3_masked_shared", 1), ("bf16_masked", 0)])
+def test_permute_large_bitmask(base, shared):
+    """A batch whose slot bitmask has >= 8192 words (4096 tokens x 64 slots) takes the
+    many-CTA slot scan; counts, offsets and row maps stay bit-exact."""
+    cfg = SMALL[base].replace(T=4096, H=128, I=128, E=64, K=4, shared=shared,
+                              M_max=(4096 if SMALL[base].layout == "masked" else 0))
+    wl = Workload(cfg)
+    L = run_permute(wl)
+    lay = oracle_layout(wl)
+    assert int(to_host(L.err)[0]) == 0
+    assert (to_host(L.masked_m) == lay["masked_m"]).all()
+    assert (to_host(L.offsets) == lay["offsets"]).all()
+    assert (to_host(L.row_of) == lay["row_of"]).all()
+    valid = lay["src_of"] >= 0
+    assert (to_host(L.src_of)[valid] == lay["src_of"][valid]).all()
+
+
 def test_permute_empty_and_one_hot():
     cfg = SMALL["e4m3_masked_shared"]
     wl = Workload(cfg)
