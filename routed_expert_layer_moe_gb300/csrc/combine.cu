@@ -30,28 +30,38 @@ __global__ void __launch_bounds__(128) combine_kernel(const TY* __restrict__ yg,
   float acc[VEC];
 #pragma unroll
   for (int i = 0; i < VEC; ++i) acc[i] = 0.0f;
-  for (int k = 0; k < KS; ++k) {
-    const int r = rows[k];
-    if (r < 0) continue;
-    const float wk = wts[k];
-    const TY* src = yg + (size_t)r * H + c0;
-    if constexpr (sizeof(TY) == 2) {
-      static_assert(VEC == 8, "bf16 path reads 16-byte vectors");
-      const uint4 raw = __ldg(reinterpret_cast<const uint4*>(src));
-      const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&raw);
+  // Up to four rows are requested before their multiply-adds (more bytes in flight per
+  // thread); the adds still run in k order, skipping rows that were not placed.
+  constexpr int B = 4;
+  for (int k0 = 0; k0 < KS; k0 += B) {
+    uint4 raw[B];
 #pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(hv[i]);
-        acc[2 * i] = fmaf(wk, f.x, acc[2 * i]);
-        acc[2 * i + 1] = fmaf(wk, f.y, acc[2 * i + 1]);
+    for (int j = 0; j < B; ++j) {
+      const int k = k0 + j;
+      if (k < KS && rows[k] >= 0) raw[j] = __ldg(reinterpret_cast<const uint4*>(yg + (size_t)rows[k] * H + c0));
+    }
+#pragma unroll
+    for (int j = 0; j < B; ++j) {
+      const int k = k0 + j;
+      if (k >= KS || rows[k] < 0) continue;
+      const float wk = wts[k];
+      if constexpr (sizeof(TY) == 2) {
+        static_assert(VEC == 8, "bf16 path reads 16-byte vectors");
+        const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&raw[j]);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const float2 f = __bfloat1622float2(hv[i]);
+          acc[2 * i] = fmaf(wk, f.x, acc[2 * i]);
+          acc[2 * i + 1] = fmaf(wk, f.y, acc[2 * i + 1]);
+        }
+      } else {
+        static_assert(VEC == 4, "fp32 path reads 16-byte vectors");
+        const float4 f = *reinterpret_cast<const float4*>(&raw[j]);
+        acc[0] = fmaf(wk, f.x, acc[0]);
+        acc[1] = fmaf(wk, f.y, acc[1]);
+        acc[2] = fmaf(wk, f.z, acc[2]);
+        acc[3] = fmaf(wk, f.w, acc[3]);
       }
-    } else {
-      static_assert(VEC == 4, "fp32 path reads 16-byte vectors");
-      const float4 f = __ldg(reinterpret_cast<const float4*>(src));
-      acc[0] = fmaf(wk, f.x, acc[0]);
-      acc[1] = fmaf(wk, f.y, acc[1]);
-      acc[2] = fmaf(wk, f.z, acc[2]);
-      acc[3] = fmaf(wk, f.w, acc[3]);
     }
   }
   TO* dst = out + (size_t)t * H + c0;
