@@ -92,8 +92,12 @@ typedef enum moe_layout { MOE_LAYOUT_MASKED = 0, MOE_LAYOUT_CONTIG = 1 } moe_lay
 
 /* Bits of the device error flag. */
 #define MOE_FLAG_OVERFLOW 1   /* a slot received more than M_max rows (masked layout); extra rows not written, their row_of is -1 */
-#define MOE_FLAG_BAD_EXPERT 2 /* an expert id outside [0,E), or one token naming an expert twice */
-#define MOE_FLAG_BAD_MAP 4    /* a physical_to_logical entry outside [0,E), or a routed expert held by no slot */
+/* an expert id outside [0,E), or one token naming an expert twice (the record
+ * with the larger k is the one not placed) */
+#define MOE_FLAG_BAD_EXPERT 2
+/* a physical_to_logical entry outside [0,E), or a routed expert held by no
+ * slot or by more than P-E+1 slots (its records are not placed) */
+#define MOE_FLAG_BAD_MAP 4
 #define MOE_FLAG_TIMEOUT 8    /* a pipeline wait inside a GEMM kernel gave up; its outputs are incomplete */
 
 /* CUDA stream, ABI-compatible with cudaStream_t. */
@@ -208,7 +212,7 @@ moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, 
  * keeps until the process exits.
  *   - A problem whose scratch exceeds 4 MiB is rejected with MOE_ERR_WORKSPACE
  *     before anything is enqueued (the scratch is (4*P*ceil(T/32) + 4) +
- *     4*P*ceil(T/32) + 4*T*K + 4*E*(P-E+1) + 4*E bytes, each term rounded up
+ *     4*P*ceil(T/32) + 4*T*K + 4*P + 4*E + 4*E bytes, each term rounded up
  *     to 256; the prefill workload T=8192, E=P=512, K=10 needs about 1.3 MiB).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call outside of any

@@ -794,20 +794,31 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   } else if (row >= __ldg(offsets + nslots)) {
     return;
   }
-  for (int c = threadIdx.x * 4; c < cols; c += blockDim.x * 4) {
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    for (int q = 0; q < ksplit; ++q) {
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)q * rows + row) * cols + c));
-      acc.x += v.x;
-      acc.y += v.y;
-      acc.z += v.z;
-      acc.w += v.w;
+  const int c = (int)(blockIdx.y * blockDim.x + threadIdx.x) * 4;  // one float4 of the row per thread
+  if (c >= cols) return;
+  // the splits are added in split order; up to eight are requested before the adds
+  constexpr int QB = 8;
+  float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+  for (int q0 = 0; q0 < ksplit; q0 += QB) {
+    float4 v[QB];
+#pragma unroll
+    for (int j = 0; j < QB; ++j)
+      if (q0 + j < ksplit)
+        v[j] = __ldcg(reinterpret_cast<const float4*>(part + ((size_t)(q0 + j) * rows + row) * cols + c));
+#pragma unroll
+    for (int j = 0; j < QB; ++j) {
+      if (q0 + j < ksplit) {
+        acc.x += v[j].x;
+        acc.y += v[j].y;
+        acc.z += v[j].z;
+        acc.w += v[j].w;
+      }
     }
-    uint2 o;
-    o.x = pack_bf16x2(acc.x, acc.y);
-    o.y = pack_bf16x2(acc.z, acc.w);
-    *reinterpret_cast<uint2*>(out + (size_t)row * cols + c) = o;
   }
+  uint2 o;
+  o.x = pack_bf16x2(acc.x, acc.y);
+  o.y = pack_bf16x2(acc.z, acc.w);
+  *reinterpret_cast<uint2*>(out + (size_t)row * cols + c) = o;
 }
 
 // ---------------------------------------------------------------------------
@@ -997,9 +1008,10 @@ int launch_reduce(const moe_problem& p, const Plan& pl, const Phase& f, const in
                   const int32_t* offsets, cudaStream_t st) {
   if (pl.ksplit <= 1) return MOE_OK;
   const long rows = (long)grouped_rows(p);
-  splitk_reduce_kernel<<<(unsigned)rows, 256, 0, st>>>(f.part, pl.ksplit, rows, f.out_cols, masked_m, offsets,
-                                                       pl.nslots, p.layout == MOE_LAYOUT_MASKED, p.M_max,
-                                                       static_cast<__nv_bfloat16*>(f.out));
+  const dim3 grid((unsigned)rows, (unsigned)((f.out_cols / 4 + 255) / 256));
+  splitk_reduce_kernel<<<grid, 256, 0, st>>>(f.part, pl.ksplit, rows, f.out_cols, masked_m, offsets, pl.nslots,
+                                             p.layout == MOE_LAYOUT_MASKED, p.M_max,
+                                             static_cast<__nv_bfloat16*>(f.out));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -127,6 +127,119 @@ def test_permute_large_bitmask(base, shared):
     assert (to_host(L.src_of)[valid] == lay["src_of"][valid]).all()
 
 
+def check_layout(L, wl, lay, values=True):
+    cfg = wl.cfg
+    assert (to_host(L.masked_m) == lay["masked_m"]).all()
+    assert (to_host(L.offsets) == lay["offsets"]).all()
+    assert (to_host(L.row_of) == lay["row_of"]).all()
+    valid = lay["src_of"] >= 0
+    src = to_host(L.src_of)
+    assert (src[valid] == lay["src_of"][valid]).all()
+    assert (src[~valid] == SENT_I32).all()
+    if values:
+        xg, xgs = oracle.dispatch_values(cfg, wl.x, lay["row_of"])
+        assert (to_host(L.xg)[valid] == xg[valid]).all()
+        if cfg.gemm == "e4m3":
+            assert (to_host(L.xg_s)[valid] == xgs[valid]).all()
+
+
+# T*K = 256: the largest batch of the one-launch permute (without a map); 4096: the largest of
+# the one-CTA layout + copy; 4100: the mark / scan / scatter sequence (single-CTA scan: 64
+# slots x 33 words)
+@pytest.mark.parametrize("T", [64, 1024, 1025])
+@pytest.mark.parametrize("base", ["e4m3_eplb_zipf", "e4m3_masked_shared", "bf16_masked", "e4m3_contig"])
+def test_permute_both_paths(base, T):
+    """Each permute path gives the oracle's layout and dispatched values, with and without a
+    replica map and a shared expert."""
+    b = SMALL[base]
+    E = 64
+    cfg = b.replace(T=T, H=256, I=128, E=E, K=4,
+                    M_max=(T if b.layout == "masked" else 0),
+                    redundant=(8 if b.redundant else 0))
+    wl = Workload(cfg)
+    L = run_permute(wl)
+    lay = oracle_layout(wl)
+    assert int(to_host(L.err)[0]) == 0
+    check_layout(L, wl, lay)
+
+
+@pytest.mark.parametrize("T", [40, 300, 1100])
+def test_permute_duplicate_expert(T):
+    """A token that names one expert twice: the record with the larger k is not placed
+    (row -1, MOE_FLAG_BAD_EXPERT) and the counts leave it out; every other record is placed
+    as the oracle places the batch without it."""
+    cfg = SMALL["e4m3_masked_shared"].replace(T=T, M_max=T)
+    wl = Workload(cfg)
+    ids = wl.ids.copy()
+    ids[3, 2] = ids[3, 0]
+    L = run_permute(wl, ids)
+    assert int(to_host(L.err)[0]) & moe.MOE_FLAG_BAD_EXPERT
+    ro = to_host(L.row_of)
+    assert ro[3, 2] == -1 and ro[3, 0] >= 0
+    # expected rows by brute force: in each slot the placed records in ascending token order
+    placed = np.ones(ids.shape, bool)
+    placed[3, 2] = False
+    want = np.full(ids.shape, -1, np.int64)
+    fill = np.zeros(cfg.E, np.int64)
+    for t in range(T):
+        for k in range(cfg.K):
+            if placed[t, k]:
+                e = ids[t, k]
+                want[t, k] = e * cfg.M_max + fill[e]
+                fill[e] += 1
+    assert (ro[:, :cfg.K] == want).all()
+    assert (ro[:, cfg.K] == cfg.E * cfg.M_max + np.arange(T)).all()  # the shared expert's rows
+    mm = to_host(L.masked_m)
+    assert (mm[:cfg.E] == fill).all() and mm[cfg.E] == T
+
+
+@pytest.mark.parametrize("T", [40, 2100])
+def test_permute_pages_replica_map(T):
+    """The EPLB page's example map [0, 1, 2, 3, 0, 1] (experts 0 and 1 in two slots each):
+    records go round-robin by token index to the replicas, as the oracle places them."""
+    cfg = SMALL["bf16_masked"].replace(T=T, E=4, K=2, M_max=T, redundant=2)
+    wl = Workload(cfg)
+    p2l = np.array([0, 1, 2, 3, 0, 1], np.int32)
+    L = wl.layer()
+    L.p2l = torch.from_numpy(p2l).cuda()
+    L.ids.copy_(torch.from_numpy(np.ascontiguousarray(wl.ids, np.int32)))
+    for t in (L.masked_m, L.offsets, L.row_of, L.src_of):
+        t.fill_(SENT_I32)
+    L.err.zero_()
+    L.permute(to_dev(wl.x))
+    torch.cuda.synchronize()
+    lay = oracle.layout(cfg, wl.ids, p2l)
+    assert lay["status"] == 0 and int(to_host(L.err)[0]) == 0
+    assert (to_host(L.masked_m) == lay["masked_m"]).all()
+    assert (to_host(L.row_of) == lay["row_of"]).all()
+    assert to_host(L.masked_m)[4] > 0 and to_host(L.masked_m)[5] > 0  # the replicas take rows
+
+
+@pytest.mark.parametrize("T", [40, 1100])
+def test_permute_bad_replica_map(T):
+    """A physical_to_logical map in which expert 0 has no slot and expert 1 has more than
+    P-E+1: MOE_FLAG_BAD_MAP, the records of both experts are not placed, the rest are."""
+    cfg = SMALL["e4m3_eplb_zipf"].replace(T=T, M_max=T)
+    wl = Workload(cfg)
+    P, E = cfg.P, cfg.E
+    p2l = np.concatenate([np.arange(E), np.ones(P - E, np.int32)]).astype(np.int32)
+    p2l[0] = 1  # expert 0 held by no slot; expert 1 by P-E+2 slots
+    L = wl.layer()
+    L.p2l = torch.from_numpy(p2l).cuda()
+    L.ids.copy_(torch.from_numpy(np.ascontiguousarray(wl.ids, np.int32)))
+    for t in (L.masked_m, L.offsets, L.row_of, L.src_of):
+        t.fill_(SENT_I32)
+    L.err.zero_()
+    L.permute(to_dev(wl.x))
+    torch.cuda.synchronize()
+    assert int(to_host(L.err)[0]) & moe.MOE_FLAG_BAD_MAP
+    ro = to_host(L.row_of)[:, :cfg.K]
+    bad = (wl.ids == 0) | (wl.ids == 1)
+    assert (ro[bad] == -1).all() and (ro[~bad] >= 0).all()
+    mm = to_host(L.masked_m)
+    assert mm[:P].sum() == (~bad).sum()
+
+
 def test_permute_empty_and_one_hot():
     cfg = SMALL["e4m3_masked_shared"]
     wl = Workload(cfg)
