@@ -10,10 +10,39 @@
 namespace moe {
 namespace {
 
-template <int PER>  // logits held per lane: E <= 32 * PER
-__global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict__ logits, int T, int E, int K,
-                                                         int32_t* __restrict__ ids, float* __restrict__ w) {
-  const int lane = threadIdx.x & 31;
+// (value, expert) a is ordered before b: larger value, or equal value and lower expert index.
+__device__ __forceinline__ bool before(float av, int ai, float bv, int bi) {
+  return av > bv || (av == bv && ai < bi);
+}
+
+// Sorts one (value, expert) pair per lane across the warp, lane 0 first in the order above
+// (a bitonic network: 15 compare-exchange stages over lane pairs).
+__device__ __forceinline__ void warp_sort(float& v, int& e, int lane) {
+#pragma unroll
+  for (int k = 2; k <= 32; k <<= 1) {
+#pragma unroll
+    for (int j = k >> 1; j > 0; j >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, j);
+      const int oe = __shfl_xor_sync(0xffffffffu, e, j);
+      const bool first = (((lane & k) == 0) == ((lane & j) == 0));  // this lane keeps the earlier one
+      if (first ? before(ov, oe, v, e) : before(v, e, ov, oe)) {
+        v = ov;
+        e = oe;
+      }
+    }
+  }
+}
+
+// PER: logits held per lane (E <= 32 * PER).  CAND (PER >= 4, large batches): the candidate
+// filter below first; it takes fewer instructions per token but a longer chain of shuffles,
+// so small batches, bound by that latency, go without it.
+template <int PER, bool CAND>
+__global__ void __launch_bounds__(256, CAND ? (PER >= 32 ? 2 : 4) : 1) route_topk_kernel(const float* __restrict__ logits, int T,
+                                                                       int E, int K, int32_t* __restrict__ ids,
+                                                                       float* __restrict__ w) {
+  __shared__ float cand_v[CAND ? 8 : 1][32];  // per warp: the candidates, when at most 32
+  __shared__ int cand_e[CAND ? 8 : 1][32];
+  const int lane = threadIdx.x & 31, wib = threadIdx.x >> 5;
   const int t = (int)((blockIdx.x * (unsigned)blockDim.x + threadIdx.x) >> 5);
   if (t >= T) return;
   const float* l = logits + (size_t)t * E;
@@ -24,6 +53,63 @@ __global__ void __launch_bounds__(256) route_topk_kernel(const float* __restrict
     const int e = lane + 32 * i;
     v[i] = (e < E) ? __ldg(l + e) : -INFINITY;
     if (e < E) avail |= 1u << i;
+  }
+  if constexpr (CAND) {
+    static_assert(PER >= 4, "every lane must hold an expert");
+    // Candidates first: tau, the K-th of the 32 lane maxima in the order above, has K
+    // elements at or before it, so every one of the top K is at or before tau.  When at most
+    // 32 elements are, they are sorted across the warp and the first K taken; otherwise the
+    // selection below runs over them.  (E > 96: every lane holds at least one expert.)
+    float mv = -INFINITY;
+    int me = 0x7fffffff;
+#pragma unroll
+    for (int i = 0; i < PER; ++i)
+      if (((avail >> i) & 1u) && (me == 0x7fffffff || v[i] > mv)) {
+        mv = v[i];
+        me = lane + 32 * i;
+      }
+    warp_sort(mv, me, lane);
+    const float tv = __shfl_sync(0xffffffffu, mv, K - 1);
+    const int te = __shfl_sync(0xffffffffu, me, K - 1);
+    uint32_t cand = 0;
+#pragma unroll
+    for (int i = 0; i < PER; ++i) {
+      const int e = lane + 32 * i;
+      if (((avail >> i) & 1u) && !before(tv, te, v[i], e)) cand |= 1u << i;
+    }
+    const int c = __popc(cand);
+    int pos = c;  // inclusive prefix over lanes
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int u = __shfl_up_sync(0xffffffffu, pos, o);
+      if (lane >= o) pos += u;
+    }
+    const int total = __shfl_sync(0xffffffffu, pos, 31);
+    avail = cand;
+    if (total <= 32) {
+      pos -= c;
+#pragma unroll
+      for (int i = 0; i < PER; ++i) {
+        if ((cand >> i) & 1u) {
+          cand_v[wib][pos] = v[i];
+          cand_e[wib][pos] = lane + 32 * i;
+          ++pos;
+        }
+      }
+      __syncwarp();
+      float sv = (lane < total) ? cand_v[wib][lane] : -INFINITY;
+      int se = (lane < total) ? cand_e[wib][lane] : 0x7fffffff;
+      warp_sort(sv, se, lane);
+      const float lmax = __shfl_sync(0xffffffffu, sv, 0);
+      const float ex = (lane < K) ? expf(sv - lmax) : 0.0f;
+      float sum = 0.0f;
+      for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, ex, k);  // fixed order k = 0..K-1
+      if (lane < K) {
+        ids[(size_t)t * K + lane] = se;
+        w[(size_t)t * K + lane] = ex / sum;
+      }
+      return;
+    }
   }
   int my_id = 0;
   float my_val = 0.0f;
@@ -69,7 +155,13 @@ template <int PER>
 void launch_route_per(const moe_problem& p, const float* logits, int32_t* ids, float* w, cudaStream_t st) {
   const int threads = 256;
   const int blocks = (int)(((int64_t)p.T * 32 + threads - 1) / threads);
-  route_topk_kernel<PER><<<blocks, threads, 0, st>>>(logits, p.T, p.E, p.K, ids, w);
+  if constexpr (PER >= 4) {
+    if (p.T >= 2048 && p.E > 96) {
+      route_topk_kernel<PER, true><<<blocks, threads, 0, st>>>(logits, p.T, p.E, p.K, ids, w);
+      return;
+    }
+  }
+  route_topk_kernel<PER, false><<<blocks, threads, 0, st>>>(logits, p.T, p.E, p.K, ids, w);
 }
 
 // "MoE inference and expert parallelism", routing section, Table 3-1 (DeepSeek-V3):

@@ -50,13 +50,17 @@ def test_route(workloads, name):
     np.testing.assert_allclose(to_host(L.w), wl.w, rtol=2e-6, atol=1e-7)
 
 
-@pytest.mark.parametrize("T,E,K", [(1, 8, 2), (37, 512, 10), (5, 256, 8), (64, 1024, 32), (3, 33, 32)])
+@pytest.mark.parametrize("T,E,K", [(1, 8, 2), (37, 512, 10), (5, 256, 8), (64, 1024, 32), (3, 33, 32),
+                                   (300, 128, 4), (7, 97, 32), (9, 96, 3),
+                                   (2048, 512, 10), (2100, 128, 32), (2050, 97, 1), (2048, 96, 8)])
 def test_route_shapes_and_ties(T, E, K):
     cfg = SMALL["tiny"].replace(T=T, E=E, K=K, M_max=T)
     logits = mi.normal(1, 77, (T, E), dtype="f32")
     logits[0, :] = 0.5                      # a token whose logits all tie
     if T > 2:
         logits[2, ::3] = logits[2, 1]       # many exact ties in another
+    if T > 1:
+        logits[1, ::max(1, E // 40)] = logits[1].max() + 1.0  # about 40 tied at the top
     ids, w = oracle.route(logits, K)
     p = moe.Problem.make(T=T, H=64, I=128, E=E, K=K, M_max=T, act="f32", wt="f32", out="f32")
     gids = torch.empty((T, K), dtype=torch.int32, device="cuda")
