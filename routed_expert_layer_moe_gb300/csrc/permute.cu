@@ -293,12 +293,13 @@ __global__ void __launch_bounds__(256) slot_scan_kernel(const uint32_t* __restri
 // Part of x[t] to its rows of the grouped buffer (`rows`: the token's K+S rows, -1 = not
 // placed): the 16-byte vectors [v_lo, v_hi) of the token's row; e4m3: quantised per 1x128
 // group on the way (16 vectors per group; v_lo and v_hi are multiples of 16).  Each thread
-// requests up to four vectors before it stores any.  All threads of the CTA take part.
+// requests up to four vectors (two when quantising) before it stores any.  All threads of the
+// CTA take part.
 template <typename TX, bool QUANT>
 __device__ __forceinline__ void copy_token(const TX* __restrict__ x, int t, int H, int KS, const int* rows,
                                            void* __restrict__ xg, float* __restrict__ xg_scales, int v_lo,
                                            int v_hi) {
-  constexpr int B = 4;
+  constexpr int B = QUANT ? 2 : 4;
   const TX* xr = x + (size_t)t * H;
   if constexpr (QUANT) {
     // 16 threads per 128-element group, 8 bf16 elements (16 bytes) each.
