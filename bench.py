@@ -30,14 +30,14 @@ import numpy as np  # noqa: E402
 
 import moe_inputs as mi  # noqa: E402
 
-HEADLINE = "mixtral_decode"
+HEADLINE = "prefill"
+# Workloads measured after the headline in the same process (the `workloads` record of the line).
+SUB_WORKLOADS = ["mixtral_decode", "dsv3_decode", "skew_eplb", "tiny", "dsv4_fp4_decode"]
 METRIC = "MoE layer tokens/s"
-# ncu DRAM bytes (read + write) per launch of the dominant kernel, keyed by the
-# workload and the hash of the kernel source they were captured from.
+# ncu DRAM bytes (read + write) per launch of a workload's dominant kernel, keyed by the
+# workload, the launch form (one-launch FFN or the gate/up launch) and the hash of the
+# kernel source the capture was taken from; a changed kernel source gives no entry (null).
 TRAFFIC = {
-    # one-launch gate/up + down kernel, ncu --set full (profiles/gemm_ffn_mixtral_decode.md):
-    # 2.821612 GB read + 6.291712 MB written
-    "mixtral_decode:ffn:b02c2d978f62c9f6": 2827903712,
 }
 
 
@@ -204,7 +204,10 @@ def expert_bytes(cfg):
     return b13, b2
 
 
-def run_gpu(args, cfg, rank, world, local_rank):
+def run_gpu(args, cfg, rank, world, local_rank, split, lite=False):
+    """Build the layer of one workload, capture its step as CUDA graphs and time `args.steps`
+    replays.  lite: the step timing alone (no end-to-end loop, no calls outside the step), for
+    the workloads measured after the headline."""
     import torch
 
     import routed_expert_layer_moe_gb300 as moe
@@ -242,11 +245,11 @@ def run_gpu(args, cfg, rank, world, local_rank):
     stream = torch.cuda.Stream(dev)
     # eager warm-up on the capture stream (first calls cache device attributes)
     with torch.cuda.stream(stream):
-        L.forward(xd, ld, stream, fused=not args.split_ffn)
+        L.forward(xd, ld, stream, fused=not split)
     stream.synchronize()
     assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
 
-    if args.split_ffn:  # gate/up and down as two launches
+    if split:  # gate/up and down as two launches
         names = ["route+permute", "gate_up", "down", "combine"]
         parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.swiglu(stream),
                  lambda: L.down(stream), lambda: L.combine(stream)]
@@ -295,6 +298,12 @@ def run_gpu(args, cfg, rank, world, local_rank):
     total_ms = ev[0][0].elapsed_time(ev[K - 1][NP])
     part_ms = {names[j]: statistics.mean(ev[i][j].elapsed_time(ev[i][j + 1]) for i in range(K)) for j in range(NP)}
     total_ms = max_over_ranks(total_ms, world, dev)
+
+    mm = L.masked_m.cpu().numpy()
+    base = dict(total_ms=total_ms, part_ms=part_ms, masked_m=mm, touched=int((mm > 0).sum()), clocks=clk.summary(),
+                n_launch=n_launch, launch_src=launch_src, x=x, logits=logits)
+    if lite:
+        return base
 
     # ---- end to end through the host: pinned inputs in, output back, every step.  A copy
     # stream moves step i+1's inputs in (and step i-1's output out) while step i computes:
@@ -362,11 +371,8 @@ def run_gpu(args, cfg, rank, world, local_rank):
     assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
 
     aux = aux_timings(moe, L, cfg, ld, stream, torch) if world == 1 else None
-    mm = L.masked_m.cpu().numpy()
-    touched = int((mm > 0).sum())
-    return dict(total_ms=total_ms, part_ms=part_ms, e2e_ms=e2e_ms, masked_m=mm, touched=touched, clocks=clk.summary(),
-                n_launch=n_launch, launch_src=launch_src, h2d=xh.numel() * xh.element_size() + lh.numel() * lh.element_size(),
-                d2h=oh.numel() * oh.element_size(), x=x, logits=logits, aux=aux)
+    return dict(base, e2e_ms=e2e_ms, h2d=xh.numel() * xh.element_size() + lh.numel() * lh.element_size(),
+                d2h=oh.numel() * oh.element_size(), aux=aux)
 
 
 def grouped_router_params(cfg):
@@ -547,6 +553,49 @@ def config_dict(cfg, n):
             else "small workload: L2-resident (launch-latency bound)"}
 
 
+def kernel_rooflines(cfg, res, peaks, split):
+    """HBM roofline of each timed GEMM part of the step: algorithmic bytes (the W13 / W2 (+ block
+    scales) of every slot with rows, the grouped activations read and written) over its
+    event-timed duration."""
+    hbm = peaks[0]
+    b13, b2 = expert_bytes(cfg)
+    rows = int(res["masked_m"].sum())
+    esz = {"f32": 4, "bf16": 2, "e4m3": 1}[cfg.gemm]
+    x_b, h_b = rows * cfg.H * esz, rows * cfg.I * esz
+    if cfg.gemm == "e4m3":
+        x_b += rows * (cfg.H // 128) * 4
+        h_b += rows * (cfg.I // 128) * 4
+    y_b = rows * cfg.H * (4 if cfg.gemm == "f32" else 2)
+    parts = {"gate_up": res["touched"] * b13 + x_b + h_b, "down": res["touched"] * b2 + h_b + y_b,
+             "gate_up+down": res["touched"] * (b13 + b2) + x_b + 2 * h_b + y_b}
+    out = {}
+    for name, algo in parts.items():
+        if name in res["part_ms"]:
+            ach = algo / (res["part_ms"][name] * 1e-3) / 1e9
+            out[name] = {"achieved_GBps": round(ach, 1), "frac": round(ach / hbm, 4), "algorithmic_bytes": int(algo),
+                         "avg_launch_us": round(res["part_ms"][name] * 1e3, 2)}
+    return out
+
+
+def summarize(cfg, res, peaks, moe_src, split, K):
+    """The measured figures of one workload: rooflines of the dominant kernel (HBM and tensor),
+    each GEMM part's HBM fraction, the step breakdown, the layer's touched-bytes rate, clocks."""
+    ms = res["total_ms"] / K
+    b13, b2 = expert_bytes(cfg)
+    layer_bytes = res["touched"] * (b13 + b2)
+    return {
+        "roofline": ffn_roofline(cfg, res, peaks, moe_src, split),
+        "roofline_tensor": tensor_roofline(cfg, res, peaks, split),
+        "kernels_hbm": kernel_rooflines(cfg, res, peaks, split),
+        "step_breakdown_us": {k: round(v * 1e3, 2) for k, v in res["part_ms"].items()},
+        "touched_slots": res["touched"],
+        "layer_hbm": {"touched_expert_bytes": int(layer_bytes),
+                      "achieved_GBps": round(layer_bytes / (ms * 1e-3) / 1e9, 1),
+                      "frac_of_peak": round(layer_bytes / (ms * 1e-3) / 1e9 / peaks[0], 4)},
+        "clocks": res["clocks"],
+    }
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -555,6 +604,8 @@ def main():
     ap.add_argument("--config", default=HEADLINE, choices=list(mi.CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="time the selected workload only (no `workloads` record of the other workloads)")
     ap.add_argument("--ffn", default="auto", choices=["auto", "fused", "split"],
                     help="gate/up and down as one launch (moe_grouped_ffn) or two; auto: one launch for bf16 "
                          "experts, two for e4m3 / e2m1 (the faster of the two on GB300 for each)")
@@ -584,37 +635,53 @@ def main():
         torch.cuda.set_device(local_rank)
         torch.distributed.init_process_group("nccl")
     peaks = load_peaks()
-    res = run_gpu(args, cfg, rank, world, local_rank)
+    moe_src = src_hash("gemm_tc.cu", "common.cuh")
+    res = run_gpu(args, cfg, rank, world, local_rank, args.split_ffn)
     if rank == 0:
         K = args.steps
-        ms = res["total_ms"] / K
         value = job_throughput(world, cfg.T, K, res["total_ms"])
         e2e = job_throughput(world, cfg.T, K, res["e2e_ms"])
-        moe_src = src_hash("gemm_tc.cu", "common.cuh")
         line = {
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": K,
-            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": cfg.gemm if cfg.wt == cfg.gemm else "%s x %s" % (cfg.wt, cfg.gemm),
+            "warmup": args.warmup, "ms_per_step": round(res["total_ms"] / K, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None,
+            "dtype": cfg.gemm if cfg.wt == cfg.gemm else "%s x %s" % (cfg.wt, cfg.gemm),
             "data": "synthetic (seeded generator, random-init experts)",
             "config": dict(config_dict(cfg, world), ffn="two launches" if args.split_ffn else "one launch"),
-            "roofline": ffn_roofline(cfg, res, peaks, moe_src, args.split_ffn),
-            "roofline_tensor": tensor_roofline(cfg, res, peaks, args.split_ffn),
-            "step_breakdown_us": {k: round(v * 1e3, 2) for k, v in res["part_ms"].items()},
-            "touched_slots": res["touched"],
+        }
+        line.update(summarize(cfg, res, peaks, moe_src, args.split_ffn, K))
+        line.update({
             "aux_calls_us": res["aux"],
             "e2e": {"value": round(e2e, 1), "unit": "tokens/s", "h2d_bytes_per_step": res["h2d"],
                     "d2h_bytes_per_step": res["d2h"]},
             "gpu_launches": res["n_launch"] * K,
             "gpu_launches_per_step": {"kernels": res["n_launch"], "counted_from": res["launch_src"]},
-            "clocks": res["clocks"],
-        }
-        b13, b2 = expert_bytes(cfg)
-        layer_bytes = res["touched"] * (b13 + b2)
-        line["layer_hbm"] = {"touched_expert_bytes": int(layer_bytes),
-                             "achieved_GBps": round(layer_bytes / (ms * 1e-3) / 1e9, 1),
-                             "frac_of_peak": round(layer_bytes / (ms * 1e-3) / 1e9 / peaks[0], 4)}
+        })
         if world == 1 and not args.no_cpu_baseline:
             line["cpu_baseline"] = cpu_baseline(cfg, res["x"], res["logits"])
+    # the other workloads, each measured in this process with the same step counts (one GPU only)
+    if world == 1 and not args.no_workloads and not args.override:
+        import torch
+        del res
+        torch.cuda.empty_cache()
+        subs = {}
+        for name in SUB_WORKLOADS:
+            if name == cfg.name:
+                continue
+            c = mi.CONFIGS[name]
+            split = args.ffn == "split" or (args.ffn == "auto" and c.gemm != "bf16")
+            r = run_gpu(args, c, rank, world, local_rank, split, lite=True)
+            K = args.steps
+            entry = {"tokens_per_s": round(job_throughput(world, c.T, K, r["total_ms"]), 1),
+                     "ms_per_step": round(r["total_ms"] / K, 4), "T": c.T, "expert_dtype": c.wt,
+                     "ffn": "two launches" if split else "one launch"}
+            entry.update(summarize(c, r, peaks, moe_src, split, K))
+            entry["gpu_launches_per_step"] = r["n_launch"]
+            subs[name] = entry
+            del r
+            torch.cuda.empty_cache()
+        line["workloads"] = subs
+    if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
         import torch

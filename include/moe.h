@@ -216,7 +216,9 @@ moe_status moe_permute(const moe_problem* p, const int32_t* ids, const void* x, 
  *     to 256; the prefill workload T=8192, E=P=512, K=10 needs about 1.3 MiB).
  *   - The first call on a device looks up the array's device address (with
  *     that device current) and keeps it; make that first call outside of any
- *     stream capture.
+ *     stream capture.  The kept address is valid for the life of the device's
+ *     primary context: do not call this entry point again after
+ *     cudaDeviceReset on that device.
  *   - All calls share the one array, which keeps the previous call's contents
  *     (the call clears what must start at zero itself).  Calls that overlap on
  *     the GPU -- on different streams, or from different threads, without

@@ -92,3 +92,33 @@ def test_host_eplb_invert_matches_oracle():
         assert r == oref and (rc == orc).all() and (l2p[:, :r] == ol2p[:, :r]).all()
     with pytest.raises(moe.MoeError):
         moe.moe_eplb_invert([0, 5], 2, 2)
+
+
+def documented_scratch_bytes(T, K, E, P):
+    """The dispatch scratch as the header states it: bitmask (+4), word prefixes, the slot of
+    each record, the compact replica list, starts and counts, each rounded up to 256 bytes."""
+    W = (T + 31) // 32
+    up = lambda b: (b + 255) // 256 * 256
+    return up(4 * P * W + 4) + up(4 * P * W) + up(4 * T * K) + up(4 * P) + up(4 * E) + up(4 * E)
+
+
+@pytest.mark.parametrize("T,K,E,P", [(8192, 10, 512, 512), (256, 8, 256, 288), (1100, 4, 64, 72), (1, 1, 8, 8),
+                                     (4096, 4, 64, 64)])
+def test_documented_scratch_formula_matches_library(T, K, E, P):
+    # fp32 problems: the GEMMs need no workspace, so moe_workspace_bytes is the dispatch's scratch alone
+    p = moe.Problem.make(T=T, H=128, I=128, E=E, K=K, P=P, layout="contig", act="f32", wt="f32", out="f32")
+    assert moe.moe_check_problem(p) == moe.MOE_OK
+    assert moe.moe_workspace_bytes(p) == documented_scratch_bytes(T, K, E, P)
+
+
+def test_no_workspace_call_rejects_beyond_four_mib_without_gpu():
+    # the size check comes before any device call; the stated prefill figure is ~1.3 MiB
+    assert abs(documented_scratch_bytes(8192, 10, 512, 512) / 2**20 - 1.3) < 0.05
+    L = moe.lib()
+    fake = ctypes.c_void_p(256)  # never dereferenced: the size check comes first
+    T = 32
+    while documented_scratch_bytes(T, 8, 1024, 1024) <= (4 << 20):
+        T += 32
+    p = moe.Problem.make(T=T, H=128, I=128, E=1024, K=8, layout="contig", act="f32", wt="f32", out="f32")
+    r = L.moe_permute_no_workspace(ctypes.byref(p), fake, fake, None, fake, fake, fake, fake, fake, None, fake, None)
+    assert r == moe.MOE_ERR_WORKSPACE

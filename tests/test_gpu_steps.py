@@ -117,18 +117,15 @@ def test_permute(workloads, name):
 @pytest.mark.parametrize("base,shared", [("e4m3_contig", 0), ("e4m3_masked_shared", 1), ("bf16_masked", 0)])
 def test_permute_large_bitmask(base, shared):
     """A batch whose slot bitmask has >= 8192 words (4096 tokens x 64 slots) takes the
-    many-CTA slot scan; counts, offsets and row maps stay bit-exact."""
-    cfg = SMALL[base].replace(T=4096, H=128, I=128, E=64, K=4, shared=shared,
+    many-CTA slot scan; counts, offsets, row maps and the dispatched rows (copies, e4m3 codes
+    and their scales) stay bit-exact, padding rows untouched."""
+    cfg = SMALL[base].replace(T=4096, H=256, I=128, E=64, K=4, shared=shared,
                               M_max=(4096 if SMALL[base].layout == "masked" else 0))
     wl = Workload(cfg)
     L = run_permute(wl)
     lay = oracle_layout(wl)
     assert int(to_host(L.err)[0]) == 0
-    assert (to_host(L.masked_m) == lay["masked_m"]).all()
-    assert (to_host(L.offsets) == lay["offsets"]).all()
-    assert (to_host(L.row_of) == lay["row_of"]).all()
-    valid = lay["src_of"] >= 0
-    assert (to_host(L.src_of)[valid] == lay["src_of"][valid]).all()
+    check_layout(L, wl, lay)
 
 
 def check_layout(L, wl, lay, values=True):
@@ -142,9 +139,13 @@ def check_layout(L, wl, lay, values=True):
     assert (src[~valid] == SENT_I32).all()
     if values:
         xg, xgs = oracle.dispatch_values(cfg, wl.x, lay["row_of"])
-        assert (to_host(L.xg)[valid] == xg[valid]).all()
+        gx = to_host(L.xg)
+        assert (gx[valid] == xg[valid]).all()
         if cfg.gemm == "e4m3":
             assert (to_host(L.xg_s)[valid] == xgs[valid]).all()
+            assert (gx[~valid] == 0x5A).all()  # padding rows untouched
+        else:
+            assert (real(gx[~valid], cfg.gemm) == -3.0).all()
 
 
 # T*K = 256: the largest batch of the one-launch permute (without a map); 4096: the largest of
