@@ -138,12 +138,26 @@ size_t moe_workspace_bytes(const moe_problem* p);
  * first MOE_STATS_BYTES of the workspace hold int32 counters
  * [2 phases][MOE_STATS_CTAS][2]: for each CTA, the units it issued (token
  * chunk x weight-tile pair x K split) and the token tiles among them (one per
- * slot and chunk of at most 128 rows).  Summed over CTAs, the token tiles of a
- * GEMM equal the sum over slots of ceil(masked_m[s] / 128).  Phase 1 is the
- * down GEMM of moe_grouped_ffn and zero otherwise.  The counters stay valid
- * until the next call that uses the workspace. */
+ * slot and chunk of at most BM rows, BM = moe_gemm_tile_rows; a GEMM that runs
+ * on SM pairs counts each pair's units once, in its first CTA).  Summed over
+ * CTAs, the token tiles of a GEMM equal the sum over slots of
+ * ceil(masked_m[s] / BM).  Phase 1 is the down GEMM of moe_grouped_ffn and
+ * zero otherwise.  The counters stay valid until the next call that uses the
+ * workspace. */
 #define MOE_STATS_CTAS 256
 #define MOE_STATS_BYTES (2 * MOE_STATS_CTAS * 2 * 4)
+
+/* Token rows BM of one tile of the tensor-core GEMM of step 3 (step = 3) or
+ * step 4 (step = 4) for this problem ("Inference INFRA methodology (5)",
+ * section "DeepGEMM": the tile height BM of the padding-waste ratio
+ * ceil(M_e / BM) * BM / M_e).  128; or 256 for FP8 / FP4 experts with at least
+ * 128 rows per slot on average (and, for step 4, H a multiple of 256): those
+ * GEMMs run on pairs of SMs (thread-block clusters of two), each SM holding 128
+ * of the tile's token rows and one of its two 128-row weight tiles, with one
+ * cta_group::2 MMA over both.  moe_grouped_ffn always uses 128-row tiles.
+ * 0 for an invalid problem or one whose GEMMs run on the CUDA cores (F32).
+ * Host only; touches no GPU. */
+int32_t moe_gemm_tile_rows(const moe_problem* p, int32_t step);
 
 /* Check a problem without touching the GPU: MOE_OK, MOE_ERR_INVALID or
  * MOE_ERR_UNSUPPORTED. */

@@ -25,6 +25,7 @@ LAYOUTS = {"masked": MOE_LAYOUT_MASKED, "contig": MOE_LAYOUT_CONTIG}
 
 # every symbol include/moe.h declares
 EXPORTS = ["moe_version", "moe_status_string", "moe_grouped_rows", "moe_workspace_bytes", "moe_check_problem",
+           "moe_gemm_tile_rows",
            "moe_route_topk", "moe_route_grouped_topk", "moe_permute", "moe_permute_no_workspace",
            "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_grouped_ffn", "moe_combine",
            "moe_eplb_record", "moe_eplb_rebalance", "moe_eplb_invert", "moe_selftest_bounded_wait"]
@@ -73,6 +74,8 @@ def lib():
     L.moe_workspace_bytes.restype = sz
     L.moe_check_problem.argtypes = [pp]
     L.moe_check_problem.restype = i32
+    L.moe_gemm_tile_rows.argtypes = [pp, i32]
+    L.moe_gemm_tile_rows.restype = i32
     L.moe_route_topk.argtypes = [pp, vp, vp, vp, vp]
     L.moe_route_topk.restype = i32
     L.moe_route_grouped_topk.argtypes = [pp, vp, vp, i32, i32, i32, ctypes.c_float, vp, vp, vp]
@@ -132,6 +135,10 @@ def moe_version() -> int:
 
 def moe_check_problem(p: Problem) -> int:
     return lib().moe_check_problem(ctypes.byref(p))
+
+
+def moe_gemm_tile_rows(p: Problem, step: int) -> int:
+    return lib().moe_gemm_tile_rows(ctypes.byref(p), step)
 
 
 def moe_grouped_rows(p: Problem) -> int:

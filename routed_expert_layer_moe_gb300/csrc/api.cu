@@ -154,6 +154,11 @@ size_t moe_workspace_bytes(const moe_problem* p) {
   return ws_bytes(*p);
 }
 
+int32_t moe_gemm_tile_rows(const moe_problem* p, int32_t step) {
+  if (check_problem(p) != MOE_OK || (step != 3 && step != 4)) return 0;
+  return gemm_tile_rows(*p, step == 3 ? MODE_SWIGLU : MODE_DOWN);
+}
+
 moe_status moe_route_topk(const moe_problem* p, const float* logits, int32_t* ids, float* w, moe_stream_t stream) {
   int r = check_problem(p);
   if (r) return (moe_status)r;

@@ -135,8 +135,11 @@ __device__ __forceinline__ int slot_rows(const TcParams& p, int s) {
 
 // srows / sbase: each slot's valid rows and first grouped-buffer row, staged in shared memory
 // at kernel start (a unit's decode then needs no global load).
+// CH: token rows of one chunk at most (BN, or 2 BN when a CTA pair shares one MMA); with a
+// pair, rank 0 takes the first half of the chunk's rows (rounded up) and rank 1 the rest.
+template <int CH = BN>
 __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, int mode, const int* prefix,
-                                            const int* srows, const int* sbase, int u) {
+                                            const int* srows, const int* sbase, int u, uint32_t rank = 0) {
   int lo = 0, hi = p.nslots;  // prefix[lo] <= u < prefix[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -149,7 +152,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
   U.s = lo;
   const int r = u - prefix[lo];
   const int m = srows[lo];
-  const int nch = (m + BN - 1) / BN;
+  const int nch = (m + CH - 1) / CH;
   U.q = r % f.ksplit;
   const int rest = r / f.ksplit;
   U.c = rest % nch;
@@ -157,6 +160,15 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
   const int base = m / nch, extra = m - base * nch;  // near-equal chunks
   U.nvalid = base + (U.c < extra ? 1 : 0);
   U.rowB = sbase[lo] + U.c * base + min(U.c, extra);
+  if constexpr (CH > BN) {
+    const int n0 = (U.nvalid + 1) >> 1;
+    if (rank) {
+      U.rowB += n0;
+      U.nvalid -= n0;
+    } else {
+      U.nvalid = n0;
+    }
+  }
   U.rowA0 = lo * f.NA + U.j * f.pair_stride;
   U.rowA1 = U.rowA0 + f.a1_off;
   U.a1 = (mode == MODE_SWIGLU) ? true : (U.j * f.pair_stride + f.a1_off < f.NA);
@@ -207,7 +219,16 @@ __device__ __forceinline__ uint32_t pack_e4m3x4(float a, float b, float c, float
   return (uint32_t)lo | ((uint32_t)hi << 16);
 }
 
-template <bool F8, int MODE, bool TM>
+// PAIR: the CTAs run as clusters of two on an SM pair (prefill-sized slots).  One unit is a
+// chunk of up to 256 token rows: each CTA stages its half of the rows (one 128-row box) and
+// one weight tile of the pair (rank 0 tile 0 = gate, rank 1 tile 1 = up), and the leader's
+// MMA thread issues one cta_group::2 MMA (M = 256 token rows, N = 256 weight rows) over both
+// CTAs' shared memory, so each SM stages 32 KB per K block instead of 48 KB for the same
+// per-SM tensor work.  Each CTA's tensor memory then holds its own rows' gate and up columns,
+// so the epilogue is the one-CTA token-major epilogue.  The MMA's completion is multicast to
+// both CTAs' barriers; the peer's copies count on the leader's stage barrier; the peer's
+// epilogue hands accumulator buffers back to the leader with cluster-scope arrivals.
+template <bool F8, int MODE, bool TM, bool PAIR = false>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB16,
                            const __grid_constant__ CUtensorMap tmB32, const __grid_constant__ CUtensorMap tmB64,
@@ -217,6 +238,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                            const TcParams p) {
   // tmA / tmB*: weights and token boxes of phase 0; tmA2 / tmC*: those of phase 1 (MODE_FFN)
   static_assert(TM || !F8, "FP8 / FP4 run token-major");
+  static_assert(!PAIR || (F8 && TM && MODE != MODE_FFN), "SM pairs: FP8 / FP4 token-major, one GEMM per launch");
+  constexpr int CH = PAIR ? 2 * BN : BN;  // token rows of one chunk at most
+  constexpr uint32_t SB = PAIR ? TILE_A_BYTES + TILE_B_BYTES : STAGE_BYTES;  // bytes of one pipeline stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
   float* sx = reinterpret_cast<float*>(smem + p.sx_off);    // [RING][BN] activation scales of one K block
@@ -229,15 +253,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint64_t* empty = full + p.stages;
   uint64_t* tfull = empty + p.stages;  // [2] accumulator buffer written
   uint64_t* tempty = tfull + 2;        // [2] accumulator buffer read
-  uint64_t* rfull = tempty + 2;        // [RING] scale slot loaded
-  uint64_t* rempty = rfull + RING;     // [RING] scale slot consumed
-  uint64_t* drain = rempty + RING;     // [1]
+  uint64_t* gfull = tempty + 2;        // [2] scale group loaded (one per half of the ring)
+  uint64_t* gempty = gfull + 2;        // [2] scale group consumed
+  uint64_t* drain = gempty + 2;        // [1]
   uint64_t* ebar = drain + 1;          // [1] all epilogue threads
+  uint64_t* fin = ebar + 1;            // [1] SM pairs: the peer CTA is done with this CTA's memory
   uint32_t* tmem_base_smem = reinterpret_cast<uint32_t*>(smem + p.misc_off);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + p.misc_off + 4);
 
   const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
+  // SM pairs: rank 0 (the leader) issues the MMAs; units are dealt per cluster
+  const uint32_t crank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = crank == 0;
+  const int unit0 = PAIR ? (int)cluster_id_x() : (int)blockIdx.x;
+  const int ustride = PAIR ? (int)nclusters_x() : (int)gridDim.x;
 
   if (tid == 0) {
     for (int i = 0; i < p.stages; ++i) {
@@ -246,20 +276,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&tfull[i], 1);
-      mbar_init(&tempty[i], EPI_WARPS);
-    }
-    for (int i = 0; i < RING; ++i) {
-      mbar_init(&rfull[i], LOAD_THREADS);
-      mbar_init(&rempty[i], EPI_WARPS);
+      mbar_init(&tempty[i], PAIR ? 2 * EPI_WARPS : EPI_WARPS);  // pairs: both CTAs' epilogue warps
+      mbar_init(&gfull[i], LOAD_THREADS);
+      mbar_init(&gempty[i], EPI_WARPS);
     }
     mbar_init(drain, 1);
     mbar_init(ebar, EPI_WARPS);
+    mbar_init(fin, 1);
     *abort_flag = 0;
     fence_barrier_init();
   }
   if (warp == 1) {
-    tmem_alloc(tmem_base_smem, TMEM_COLS);
-    tmem_relinquish();
+    tmem_alloc<PAIR>(tmem_base_smem, TMEM_COLS);
+    tmem_relinquish<PAIR>();
   }
   // unit counts per slot -> prefix (one list per phase; the units of phase 1 follow phase 0's)
   constexpr int NPH = (MODE == MODE_FFN) ? 2 : 1;
@@ -268,7 +297,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int m = slot_rows(p, s);
     srows[s] = m;
     sbase[s] = p.masked ? s * p.M_max : __ldg(p.offsets + s);
-    const int nch = (m + BN - 1) / BN;
+    const int nch = (m + CH - 1) / CH;
 #pragma unroll
     for (int h = 0; h < NPH; ++h) prefix[h * pstride + s + 1] = nch * p.ph[h].pairs * p.ph[h].ksplit;
   }
@@ -294,6 +323,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
   __syncthreads();
+  // SM pairs: both CTAs' barriers are initialised before either CTA touches the other's
+  if constexpr (PAIR) cluster_sync_all();
   tc_fence_after_sync();
   const uint32_t tmem_base = *tmem_base_smem;
   const int total0 = prefix[p.nslots];
@@ -319,7 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   auto locate = [&](int u, int& h, int& mode) -> Unit {
     h = (MODE == MODE_FFN && u >= total0) ? 1 : 0;
     mode = (MODE == MODE_FFN) ? p.ph[h].mode : MODE;
-    return decode_unit(p, p.ph[h], mode, prefix + h * pstride, srows, sbase, h ? u - total0 : u);
+    return decode_unit<CH>(p, p.ph[h], mode, prefix + h * pstride, srows, sbase, h ? u - total0 : u, crank);
   };
 
   if (warp < EPI_WARP0) {
@@ -346,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         // Two-phase launch: a down unit's first stage requests its weight tiles first and its
         // token tile (rows of h) only once the slot's gate/up units have released them.
-        for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        for (int u = unit0; ok && u < total; u += ustride) {
           int h, mode;
           const Unit U = locate(u, h, mode);
           const CUtensorMap* ma = h ? &tmA2 : &tmA;
@@ -365,15 +396,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           bool check_ready = (MODE == MODE_FFN) && h == 1;
-          const uint32_t bytes = p.a_tile_tx * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
+          // SM pairs: the leader's stage barrier counts both CTAs' copies (a token box and one
+          // weight tile each); the peer's own stage barriers are not used
+          const uint32_t bytes = PAIR ? 2u * (p.a_tile_tx + (uint32_t)BN * ROW_BYTES)
+                                      : p.a_tile_tx * (U.a1 ? 2u : 1u) + (uint32_t)box * ROW_BYTES;
           for (int kb = U.kb0; kb < U.kb1; ++kb) {
             if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag, TIMEOUT)) {
               ok = false;
               break;
             }
-            uint8_t* st = smem + (size_t)stage * STAGE_BYTES;
-            mbar_arrive_expect_tx(&full[stage], bytes);
+            uint8_t* st = smem + (size_t)stage * SB;
             const int x = kb * kb_elems;
+            if constexpr (PAIR) {
+              // stage = [this CTA's 128 token rows | its weight tile]: rank 0 holds tile 0 and rank 1
+              // tile 1, the two halves of the N = 256 pair MMA's B operand
+              if (leader) {
+                mbar_arrive_expect_tx(&full[stage], bytes);
+                tma_load_2d(st, mb, &full[stage], x, U.rowB);
+                tma_load_2d_hint(st + TILE_B_BYTES, ma, &full[stage], x, U.rowA0, pol);
+              } else {
+                const uint32_t lbar = mapa_shared(&full[stage], 0);
+                tma_load_2d_pair(st, mb, lbar, x, U.rowB);
+                tma_load_2d_pair_hint(st + TILE_B_BYTES, ma, lbar, x, U.rowA1, pol);
+              }
+              ++issued;
+              if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
+            mbar_arrive_expect_tx(&full[stage], bytes);
             tma_load_2d_hint(st, ma, &full[stage], x, U.rowA0, pol);
             if (U.a1) tma_load_2d_hint(st + TILE_A_BYTES, ma, &full[stage], x, U.rowA1, pol);
             if (check_ready) {
@@ -389,7 +442,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!ok) break;
           }
         }
-        if (!ok) {
+        if (!ok && PAIR && !leader) {
+          // the peer's copies count on the leader's barriers: give those in flight time to land
+          const uint64_t t0 = global_timer_ns();
+          while (global_timer_ns() - t0 < 200000u) {
+          }
+        } else if (!ok) {
           // let the copies already in flight land before the CTA's shared memory is released
           const long first = issued > p.stages ? issued - p.stages : 0;
           for (long i = first; i < issued; ++i) {
@@ -410,16 +468,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         bool ok = true;
         bool any = false;
         int units[2] = {0, 0}, tiles[2] = {0, 0};
-        for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+        // SM pairs: the leader issues every MMA of the pair; the peer's thread only reports zeros
+        for (int u = unit0; ok && leader && u < total; u += ustride) {
           int h, mode;
           const Unit U = locate(u, h, mode);
           ++units[h];
           tiles[h] += (U.j == 0 && U.q == 0);  // one unit per (slot, token chunk) has j = q = 0
           // weight-major: M = 128 weight rows, N = tokens rounded to 16 (one MMA per tile);
-          // token-major: M = 128 token rows, N = both weight tiles (one MMA)
+          // token-major: M = 128 token rows, N = both weight tiles (one MMA); SM pairs: M = 256
+          // token rows over both CTAs, N = 256 (each CTA holds one weight tile)
           // (token-major: the weights are the B operand, of format w_fmt)
-          const uint32_t idesc = TM ? (mma_idesc<F8>(BM, U.a1 ? 2 * BM : BM) | (p.w_fmt << 10))
-                                    : mma_idesc<F8>(BM, (U.nvalid + 15) & ~15);
+          // (token-major FP8 / FP4: the weights are the B operand, of format w_fmt)
+          const uint32_t idesc = PAIR ? (mma_idesc<F8>(2 * BM, 2 * BM) | (p.w_fmt << 10))
+                                 : TM ? (mma_idesc<F8>(BM, U.a1 ? 2 * BM : BM) | (F8 ? p.w_fmt << 10 : 0u))
+                                      : mma_idesc<F8>(BM, (U.nvalid + 15) & ~15);
           uint32_t b = 0;
           if constexpr (!F8) {
             b = acc_it & 1u;
@@ -430,18 +492,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_after_sync();
           }
           for (int kb = U.kb0; kb < U.kb1; ++kb) {
-            if constexpr (F8) {
-              b = acc_it & 1u;
-              if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
-                ok = false;
-                break;
-              }
-            }
             if (!mbar_wait(&full[stage], phase, abort_flag, TIMEOUT)) {
               ok = false;
               break;
             }
             tc_fence_after_sync();
+            if constexpr (F8) {
+              // FP8 / FP4 (token-major): one N = 256 MMA group per K block (tile 0 = gate or the
+              // first down tile in columns 0-127 of buffer b, tile 1 in 128-255), a fresh partial
+              // sum per block for the epilogue's promotion
+              b = acc_it & 1u;
+              if (!mbar_wait(&tempty[b], ((acc_it >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after_sync();
+              const uint32_t st = smem_u32(smem + (size_t)stage * SB);
+              // one CTA: [tile 0 | tile 1 | tokens]; pairs: [tokens | this CTA's weight tile]
+              const uint64_t dtok = smem_desc_sw128(PAIR ? st : st + 2 * TILE_A_BYTES);
+              const uint64_t dw = smem_desc_sw128(PAIR ? st + TILE_B_BYTES : st);
+              const uint32_t d0 = tmem_base + b * 256u;
+#pragma unroll
+              for (int ks = 0; ks < 4; ++ks) {
+                if constexpr (PAIR)
+                  tc_mma_pair_f8(d0, dtok + 2 * ks, dw + 2 * ks, idesc, ks > 0);
+                else
+                  tc_mma<true>(d0, dtok + 2 * ks, dw + 2 * ks, idesc, ks > 0);
+              }
+              any = true;
+              if constexpr (PAIR) {
+                tc_commit_pair(&empty[stage], 3);  // both CTAs' stages are free
+                tc_commit_pair(&tfull[b], 3);      // both CTAs' accumulators are written
+              } else {
+                tc_commit(&empty[stage]);
+                tc_commit(&tfull[b]);
+              }
+              ++acc_it;
+              if (++stage == p.stages) {
+                stage = 0;
+                phase ^= 1u;
+              }
+              continue;
+            }
             const uint32_t st = smem_u32(smem + (size_t)stage * STAGE_BYTES);
             const uint64_t dw0 = smem_desc_sw128(st);
             const uint64_t dw1 = smem_desc_sw128(st + TILE_A_BYTES);
@@ -459,10 +551,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             any = true;
             tc_commit(&empty[stage]);
-            if constexpr (F8) {
-              tc_commit(&tfull[b]);
-              ++acc_it;
-            }
             if (++stage == p.stages) {
               stage = 0;
               phase ^= 1u;
@@ -492,7 +580,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         if (!ok && any) {
           // all MMAs issued by this thread must finish before tensor memory is freed
-          tc_commit(drain);
+          if constexpr (PAIR)
+            tc_commit_pair(drain, 1);
+          else
+            tc_commit(drain);
           const long long t0 = clock64();
           while (!mbar_try_wait(drain, 0) && clock64() - t0 < TIMEOUT) {
           }
@@ -500,29 +591,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     } else if (F8) {
       // ------------------------------------------------------------ FP8 scale loaders
-      // Fill the scale ring SG K blocks per pass with asynchronous 4-byte copies: the
-      // loaders never wait for data, so the ring runs up to RING blocks ahead of the
-      // epilogue.  Each slot's rfull barrier completes when the copies issued before
-      // its arrival by all loader threads have landed.
+      // The activation and weight scales of up to SG K blocks per group go into one half of
+      // a two-group ring in shared memory with asynchronous 4-byte copies; the loaders never
+      // wait for data, so the ring runs a group ahead of the epilogue.  The group's gfull
+      // barrier completes when the copies issued by all loader threads have landed; the
+      // epilogue waits on it once per group and releases the half once per group, so the
+      // scales cost it no barrier operation per K block.
       const int lt = tid - LOAD_WARP0 * 32;
-      uint32_t g = 0;  // K blocks staged so far
+      uint32_t gi = 0;  // groups staged so far
       bool ok = true;
-      for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
+      for (int u = unit0; ok && u < total; u += ustride) {
         int h, mode;
         const Unit U = locate(u, h, mode);
         const Phase& f = p.ph[h];
         const int ra0 = U.rowA0 / BM, ra1 = U.rowA1 / BM;
         bool check_ready = (MODE == MODE_FFN) && h == 1;  // h scales of a down unit: written by gate/up units
-        for (int k0 = U.kb0; ok && k0 < U.kb1; k0 += SG) {
+        for (int k0 = U.kb0; ok && k0 < U.kb1; k0 += SG, ++gi) {
           const int nk = min(SG, U.kb1 - k0);
-          for (int j = 0; j < nk; ++j) {
-            const uint32_t gj = g + j;
-            if (!mbar_wait(&rempty[gj % RING], ((gj / RING) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
-              ok = false;
-              break;
-            }
+          const uint32_t gh = gi & 1u;  // half of the ring
+          if (!mbar_wait(&gempty[gh], ((gi >> 1) & 1u) ^ 1u, abort_flag, TIMEOUT)) {
+            ok = false;
+            break;
           }
-          if (!ok) break;
           if (check_ready) {
             check_ready = false;
             if (!wait_ready(U.s)) {
@@ -530,20 +620,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
           }
+          float* sxg = sx + gh * SG * BN;  // [SG][BN]
+          float* swg = sw + gh * SG * 2;   // [SG][2 tiles]
           // activation scales of the chunk's rows: element (c, j) = b_scales[rowB + c][k0 + j]
           const int n = U.nvalid * nk;
           for (int idx = lt; idx < n; idx += LOAD_THREADS) {
             const int c = idx / nk, j = idx - c * nk;
-            cp_async4(sx + ((g + j) % RING) * BN + c, f.b_scales + (size_t)(U.rowB + c) * f.scale_cols + k0 + j);
+            cp_async4(sxg + j * BN + c, f.b_scales + (size_t)(U.rowB + c) * f.scale_cols + k0 + j);
           }
           // weight block scales of the two tiles (a missing second tile's value is never used)
           for (int idx = lt; idx < 2 * nk; idx += LOAD_THREADS) {
             const int j = idx >> 1, t = idx & 1;
             if (t == 0 || U.a1)
-              cp_async4(sw + ((g + j) % RING) * 2 + t, f.a_scales + (size_t)(t ? ra1 : ra0) * f.scale_cols + k0 + j);
+              cp_async4(swg + j * 2 + t, f.a_scales + (size_t)(t ? ra1 : ra0) * f.scale_cols + k0 + j);
           }
-          for (int j = 0; j < nk; ++j) cp_async_arrive_noinc(&rfull[(g + j) % RING]);
-          g += nk;
+          cp_async_arrive_noinc(&gfull[gh]);
         }
       }
       cp_async_wait_all();  // no copy may land after the CTA has exited
@@ -555,7 +646,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int half = (warp - EPI_WARP0) >> 2; // column half (warpgroup 1 or 2)
     const int lrow = quarter * 32 + lane;     // tensor-memory lane of this thread
     const uint32_t t_lane = tmem_base + ((uint32_t)(quarter * 32) << 16);
-    uint32_t acc_it = 0, r_it = 0, u_it = 0;
+    uint32_t acc_it = 0, g_it = 0, u_it = 0;
     uint32_t ephase = 0;
     bool ok = true;
     // one arrival per warp, after the warp's own threads are ordered by __syncwarp
@@ -582,7 +673,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ephase ^= 1u;
       return r;
     };
-    for (int u = blockIdx.x; ok && u < total; u += gridDim.x, ++u_it) {
+    for (int u = unit0; ok && u < total; u += ustride, ++u_it) {
       int h, mode;
       const Unit U = locate(u, h, mode);
       const Phase& f = p.ph[h];
@@ -604,8 +695,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
       if constexpr (F8) {
         for (int k = 0; k < nkb; ++k) {
-          const uint32_t slot = r_it % RING;
-          if (!mbar_wait(&rfull[slot], (r_it / RING) & 1u, abort_flag, TIMEOUT)) {
+          const int j = k % SG;  // K block within its scale group (groups restart with each unit)
+          const uint32_t gh = g_it & 1u;  // half of the scale ring
+          if (j == 0 && !mbar_wait(&gfull[gh], (g_it >> 1) & 1u, abort_flag, TIMEOUT)) {
             ok = false;
             break;
           }
@@ -615,29 +707,33 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             break;
           }
           tc_fence_after_sync();
-          const float* sxs = sx + slot * BN;
-          const float s0 = sw[slot * 2], s1 = sw[slot * 2 + 1];
-          if constexpr (TM) {
-            const float xs = sxs[lrow];
-            const float p0 = s0 * xs, p1 = s1 * xs;
+          const int slot = (int)gh * SG + j;
+          const float xs = sx[slot * BN + lrow];
+          const float p0 = sw[slot * 2] * xs, p1 = sw[slot * 2 + 1] * xs;
 #pragma unroll
-            for (int pr = 0; pr < 2; ++pr) {
-              float v0[32], v1[32];
-              const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
-              tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
-              if (pr == 1) {  // the buffer is read: hand it back before the last multiply-adds
-                tc_fence_before_sync();
+          for (int pr = 0; pr < 2; ++pr) {
+            float v0[32], v1[32];
+            const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
+            tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
+            if (pr == 1) {  // the buffer is read: hand it back before the last multiply-adds
+              tc_fence_before_sync();
+              if (PAIR && !leader) {  // to the leader's MMA thread, which waits on its own barrier
+                __syncwarp();
+                if (lane == 0) mbar_arrive_remote(mapa_shared(&tempty[b], 0));
+              } else {
                 warp_arrive(&tempty[b]);
               }
+            }
 #pragma unroll
-              for (int i = 0; i < 32; i += 2) {
-                fma2(acc0[pr * 32 + i], acc0[pr * 32 + i + 1], v0[i], v0[i + 1], p0);
-                fma2(acc1[pr * 32 + i], acc1[pr * 32 + i + 1], v1[i], v1[i + 1], p1);
-              }
+            for (int i = 0; i < 32; i += 2) {
+              fma2(acc0[pr * 32 + i], acc0[pr * 32 + i + 1], v0[i], v0[i + 1], p0);
+              fma2(acc1[pr * 32 + i], acc1[pr * 32 + i + 1], v1[i], v1[i + 1], p1);
             }
           }
-          warp_arrive(&rempty[slot]);  // this block's scales are no longer read
-          ++r_it;
+          if (j == SG - 1 || k == nkb - 1) {  // the group's scales are no longer read
+            warp_arrive(&gempty[gh]);
+            ++g_it;
+          }
           ++acc_it;
         }
         if (!ok) break;
@@ -774,9 +870,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before_sync();
   __syncthreads();
+  if constexpr (PAIR) {
+    // Neither CTA of the pair frees its tensor memory or leaves while the other may still use
+    // it: the leader's MMAs read the peer's shared memory and write its tensor memory, the
+    // peer's copies and buffer releases land on the leader's barriers.  Each CTA tells the
+    // other it is done (all of its roles have finished above) and waits, bounded, for the
+    // other's word.
+    if (tid == 0) {
+      mbar_arrive_remote(mapa_shared(fin, crank ^ 1u));
+      const long long t0 = clock64();
+      while (!mbar_try_wait<true>(fin, 0)) {
+        if (clock64() - t0 > TIMEOUT) {
+          *abort_flag = 1;
+          break;
+        }
+      }
+    }
+    __syncthreads();
+  }
   if (warp == 1) {
     tc_fence_after_sync();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    tmem_dealloc<PAIR>(tmem_base, TMEM_COLS);
   }
   if (tid == 0 && *abort_flag) atomicOr(p.err, MOE_FLAG_TIMEOUT);
 }
@@ -828,10 +942,20 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
 struct Plan {
   int ksplit, kb_per_split, kb_total, stages, nslots, pairs;
   bool tm;
+  bool pair;  // clusters of two CTAs sharing cta_group::2 MMAs over 256-row token chunks
   size_t smem;
   uint32_t sx_off, sw_off, red_off, pre_off, bar_off, misc_off;
   size_t part_bytes;
 };
+
+// SM pairs for FP8 / FP4 slots of prefill size (128 rows or more on average): one 256-row
+// chunk per slot instead of two 128-row chunks that each stage the slot's weight tiles, and
+// 32 KB stages (each SM holds its token rows and one weight tile).  The down GEMM needs
+// whole pairs of weight tiles (H a multiple of 256); the one-launch FFN stays on single CTAs.
+bool use_pairs(const moe_problem& p, int mode, int nphase) {
+  const double rows_per_slot = (double)p.T * p.K / std::max(1, p.P);
+  return fp8_acts(p) && nphase == 1 && rows_per_slot >= 128.0 && (mode == MODE_SWIGLU || p.H % 256 == 0);
+}
 
 Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int nphase = 1) {
   Plan pl{};
@@ -848,6 +972,7 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int n
   // needs no promotion; there weight-major is kept for decode-sized experts.
   const double rows_per_slot = (double)p.T * p.K / std::max(1, p.P);
   pl.tm = f8 || rows_per_slot >= 64.0;
+  pl.pair = use_pairs(p, mode, nphase);
   // upper bound of the token chunks over all slots
   long chunks;
   if (p.layout == MOE_LAYOUT_MASKED) {
@@ -858,7 +983,7 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int n
   }
   const long tiles = chunks * pl.pairs;
   pl.ksplit = 1;
-  if (mode == MODE_DOWN && tiles > 0 && tiles < 3L * sm_count) {
+  if (mode == MODE_DOWN && !pl.pair && tiles > 0 && tiles < 3L * sm_count) {
     // split K so the unit count fills whole waves; keep >= 4 K blocks per split
     double best = 0.0;
     for (int ks = 1; ks <= 16 && pl.kb_total / ks >= 4; ++ks) {
@@ -895,13 +1020,14 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int n
   const size_t red_b = (size_t)2 * 512 * 4;
   const size_t pre_b = ((size_t)nphase * (pl.nslots + 1) + 2 * (size_t)pl.nslots) * 4;  // prefix, rows, bases
   pl.stages = 0;
-  for (int st = 6; st >= 2; --st) {
-    extra = (size_t)st * STAGE_BYTES;
+  const size_t stage_bytes = pl.pair ? (size_t)(TILE_A_BYTES + TILE_B_BYTES) : (size_t)STAGE_BYTES;
+  for (int st = 8; st >= 2; --st) {
+    extra = (size_t)st * stage_bytes;
     pl.sx_off = (uint32_t)carve(sx_b, 16);
     pl.sw_off = (uint32_t)carve(sw_b, 16);
     pl.red_off = (uint32_t)carve(red_b, 16);
     pl.pre_off = (uint32_t)carve(pre_b, 16);
-    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 2 * RING + 8) * 8, 8);
+    pl.bar_off = (uint32_t)carve((size_t)(2 * st + 16) * 8, 8);
     pl.misc_off = (uint32_t)carve(16, 16);
     const size_t total = extra + 1024;
     if ((int)total <= smem_cap) {
@@ -916,9 +1042,9 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int n
 
 // Register split and shared-memory limit of one kernel instantiation, checked once per device
 // (the flags are per instantiation: all of them share one function type).
-template <bool F8, int MODE, bool TM>
+template <bool F8, int MODE, bool TM, bool PAIR = false>
 int prepare_kernel() {
-  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM>;
+  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM, PAIR>;
   const int needed_regs = Regs<F8>::needed;
   static bool attr_set[64] = {};
   int dev = 0;
@@ -1015,12 +1141,40 @@ int launch_reduce(const moe_problem& p, const Plan& pl, const Phase& f, const in
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
-template <bool F8, int MODE, bool TM>
+// Clusters of two that the device keeps resident at once for the SM-pair kernel (its shared
+// memory allows one CTA per SM), queried once per device and instantiation.
+template <bool F8, int MODE>
+int pair_clusters(size_t smem) {
+  static int n[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 64 && n[dev] > 0) return n[dev];
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(2 * (device_info().sm_count / 2));
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = smem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int c = 0;
+  if (cudaOccupancyMaxActiveClusters(&c, grouped_gemm_tc_kernel<F8, MODE, true, true>, &cfg) != cudaSuccess ||
+      c <= 0)
+    return 0;
+  c = std::min(c, device_info().sm_count / 2);
+  if (dev < 64) n[dev] = c;
+  return c;
+}
+
+template <bool F8, int MODE, bool TM, bool PAIR = false>
 int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float* act_scales, const void* w,
               const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
               int32_t* err, void* ws, cudaStream_t st) {
-  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM>;
-  int r = prepare_kernel<F8, MODE, TM>();
+  auto kern = grouped_gemm_tc_kernel<F8, MODE, TM, PAIR>;
+  int r = prepare_kernel<F8, MODE, TM, PAIR>();
   if (r) return r;
   CUtensorMap tA, tB[4];
   r = make_maps(p, MODE, act, w, tA, tB);
@@ -1030,8 +1184,28 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
   prm.ph[0] = make_phase(p, MODE, pl, act_scales, w_scales, out, out_scales,
                          reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + STATS_BYTES));
   prm.ph[1] = prm.ph[0];
-  kern<<<device_info().sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], tA, tB[0], tB[1],
-                                                             tB[2], tB[3], prm);
+  if constexpr (PAIR) {
+    const int nc = pair_clusters<F8, MODE>(pl.smem);
+    if (nc <= 0) return MOE_ERR_CUDA;
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(2 * nc);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = pl.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, kern, tA, tB[0], tB[1], tB[2], tB[3], tA, tB[0], tB[1], tB[2], tB[3], prm) !=
+        cudaSuccess)
+      return MOE_ERR_CUDA;
+  } else {
+    kern<<<device_info().sm_count, NUM_THREADS, pl.smem, st>>>(tA, tB[0], tB[1], tB[2], tB[3], tA, tB[0], tB[1],
+                                                               tB[2], tB[3], prm);
+  }
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
   return launch_reduce(p, pl, prm.ph[0], masked_m, offsets, st);
 }
@@ -1132,6 +1306,11 @@ __global__ void __launch_bounds__(256) grouped_gemm_f32_kernel(const float* __re
 
 }  // namespace
 
+int gemm_tile_rows(const moe_problem& p, int mode) {
+  if (p.wt == MOE_F32) return 0;
+  return use_pairs(p, mode, 1) ? 2 * BN : BN;
+}
+
 size_t gemm_workspace_bytes(const moe_problem& p) {
   if (p.wt == MOE_F32) return 0;
   // Split-K state depends on the SM count; size it for the largest plausible GPU (up to 256 SMs).
@@ -1175,6 +1354,13 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
   return launch_tc<F8_, MODE_, TM_>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err, \
                                     ws, st)
   if (f8) {
+    if (pl.pair) {
+      if (mode == MODE_SWIGLU)
+        return launch_tc<true, MODE_SWIGLU, true, true>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out,
+                                                        out_scales, err, ws, st);
+      return launch_tc<true, MODE_DOWN, true, true>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out,
+                                                    out_scales, err, ws, st);
+    }
     if (mode == MODE_SWIGLU) MOE_LAUNCH(true, MODE_SWIGLU, true);
     MOE_LAUNCH(true, MODE_DOWN, true);
   }

@@ -392,13 +392,16 @@ def test_grouped_ffn_one_launch(workloads, name):
 @pytest.mark.parametrize("name", [n for n in NAMES if SMALL[n].gemm != "f32"])
 def test_gemm_issue_counters(workloads, name):
     """The GEMMs' token tiles (summed over CTAs from the counters in the workspace) equal the
-    oracle's sum over slots of ceil(masked_m / 128): no tile for padding rows or empty slots;
-    every unit belongs to one such tile (units = tiles x tile pairs x K splits)."""
+    oracle's sum over slots of ceil(masked_m / BM), BM the GEMM's tile height (128, or 256 on SM
+    pairs): no tile for padding rows or empty slots; every unit belongs to one such tile
+    (units = tiles x tile pairs x K splits).  The one-launch FFN uses 128-row tiles."""
     wl = workloads[name]
     cfg = wl.cfg
     lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
-    want = oracle.token_tiles(lay["masked_m"], 128)
     L = wl.layer()
+    bm = {3: moe.moe_gemm_tile_rows(L.p, 3), 4: moe.moe_gemm_tile_rows(L.p, 4)}
+    assert bm[3] in (128, 256) and bm[4] in (128, 256)
+    want = oracle.token_tiles(lay["masked_m"], 128)
     L.xg.copy_(to_dev(xg))
     if xgs is not None:
         L.xg_s.copy_(to_dev(xgs))
@@ -410,11 +413,12 @@ def test_gemm_issue_counters(workloads, name):
         c = L.ws[:moe.MOE_STATS_BYTES].view(torch.int32).cpu().numpy().reshape(2, moe.MOE_STATS_CTAS, 2)
         return c.sum(axis=1)  # [phase][units, tiles]
 
-    for call in (L.swiglu, L.down):
+    for step, call in ((3, L.swiglu), (4, L.down)):
         call()
         c = counters()
-        assert c[0, 1] == want and c[1].sum() == 0
-        assert c[0, 0] % max(want, 1) == 0 and c[0, 0] >= want
+        want_s = oracle.token_tiles(lay["masked_m"], bm[step])
+        assert c[0, 1] == want_s and c[1].sum() == 0
+        assert c[0, 0] % max(want_s, 1) == 0 and c[0, 0] >= want_s
     L.ffn()
     c = counters()
     assert c[0, 1] == want and c[1, 1] == want
