@@ -196,21 +196,6 @@ __device__ __forceinline__ void cluster_sync_all() {
 
 // ---- packed fp32 arithmetic ----
 
-// (a0, a1) += (x0, x1) * s as one packed fp32x2 multiply-add: the same two roundings as two
-// fmaf calls, in one instruction.
-__device__ __forceinline__ void fma2(float& a0, float& a1, float x0, float x1, float s) {
-  asm("{\n"
-      "  .reg .b64 d, x, sv, c;\n"
-      "  mov.b64 x, {%2, %3};\n"
-      "  mov.b64 sv, {%4, %4};\n"
-      "  mov.b64 c, {%0, %1};\n"
-      "  fma.rn.f32x2 d, x, sv, c;\n"
-      "  mov.b64 {%0, %1}, d;\n"
-      "}\n"
-      : "+f"(a0), "+f"(a1)
-      : "f"(x0), "f"(x1), "f"(s));
-}
-
 // ---- wide stores ----
 
 // One 32-byte store (a full L2 sector); dst must be 32-byte aligned.
@@ -412,6 +397,38 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)
   for (int i = 0; i < 32; ++i) {
     a[i] = __uint_as_float(r[i]);
     b[i] = __uint_as_float(r[32 + i]);
+  }
+}
+
+// One 32-lane x 32-column fp32 load from tensor memory, not waited for: the registers hold the
+// values only after tmem_wait_ld32 on the same array (which names them as operands, so the
+// compiler cannot read them earlier).
+__device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(ta)
+      : "memory");
+}
+
+// Wait for this thread's tensor-memory loads; r is the array the last load wrote.
+__device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.wait::ld.sync.aligned;\n"
+      : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]), "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]), "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]), "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+      :
+      : "memory");
+}
+
+// a[o .. o+31] += r[0..31] * s, as sixteen packed fp32x2 multiply-adds (two fmaf roundings each).
+__device__ __forceinline__ void fma2_chunk(float* a, const uint32_t (&r)[32], float s) {
+  const float2 sv = make_float2(s, s);
+#pragma unroll
+  for (int i = 0; i < 32; i += 2) {
+    const float2 v = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sv,
+                                make_float2(a[i], a[i + 1]));
+    a[i] = v.x;
+    a[i + 1] = v.y;
   }
 }
 

@@ -710,26 +710,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const int slot = (int)gh * SG + j;
           const float xs = sx[slot * BN + lrow];
           const float p0 = sw[slot * 2] * xs, p1 = sw[slot * 2 + 1] * xs;
-#pragma unroll
-          for (int pr = 0; pr < 2; ++pr) {
-            float v0[32], v1[32];
-            const uint32_t col = b * 256u + (uint32_t)(c_lo + pr * 32);
-            tmem_ld32x2(t_lane + col, t_lane + col + 128u, v0, v1);
-            if (pr == 1) {  // the buffer is read: hand it back before the last multiply-adds
-              tc_fence_before_sync();
-              if (PAIR && !leader) {  // to the leader's MMA thread, which waits on its own barrier
-                __syncwarp();
-                if (lane == 0) mbar_arrive_remote(mapa_shared(&tempty[b], 0));
-              } else {
-                warp_arrive(&tempty[b]);
-              }
-            }
-#pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-              fma2(acc0[pr * 32 + i], acc0[pr * 32 + i + 1], v0[i], v0[i + 1], p0);
-              fma2(acc1[pr * 32 + i], acc1[pr * 32 + i + 1], v1[i], v1[i + 1], p1);
-            }
+          // four 32-column chunks (tile 0 cols c_lo.., tile 1 cols c_lo.., tile 0 cols c_lo+32..,
+          // tile 1 cols c_lo+32..), each load issued before the multiply-adds of the previous
+          // chunk so that its latency hides behind them
+          uint32_t ra[32], rb[32];
+          const uint32_t c0 = t_lane + b * 256u + (uint32_t)c_lo;
+          tmem_ld32(c0, ra);
+          tmem_wait_ld32(ra);
+          tmem_ld32(c0 + 128u, rb);
+          fma2_chunk(acc0, ra, p0);
+          tmem_wait_ld32(rb);
+          tmem_ld32(c0 + 32u, ra);
+          fma2_chunk(acc1, rb, p1);
+          tmem_wait_ld32(ra);
+          tmem_ld32(c0 + 160u, rb);
+          fma2_chunk(acc0 + 32, ra, p0);
+          tmem_wait_ld32(rb);
+          // the buffer is read: hand it back before the last multiply-adds
+          tc_fence_before_sync();
+          if (PAIR && !leader) {  // to the leader's MMA thread, which waits on its own barrier
+            __syncwarp();
+            if (lane == 0) mbar_arrive_remote(mapa_shared(&tempty[b], 0));
+          } else {
+            warp_arrive(&tempty[b]);
           }
+          fma2_chunk(acc1 + 32, rb, p1);
           if (j == SG - 1 || k == nkb - 1) {  // the group's scales are no longer read
             warp_arrive(&gempty[gh]);
             ++g_it;
