@@ -31,6 +31,7 @@ import numpy as np  # noqa: E402
 import moe_inputs as mi  # noqa: E402
 
 HEADLINE = "prefill"
+FFN_PART = "gate_up+down+combine"  # the moe_ffn_combine call of the one-launch step
 # Workloads measured after the headline in the same process (the `workloads` record of the line).
 SUB_WORKLOADS = ["mixtral_decode", "dsv3_decode", "skew_eplb", "tiny", "dsv4_fp4_decode"]
 METRIC = "MoE layer tokens/s"
@@ -249,14 +250,14 @@ def run_gpu(args, cfg, rank, world, local_rank, split, lite=False):
     stream.synchronize()
     assert int(L.err.item()) == 0, "device error flag %d" % int(L.err.item())
 
-    if split:  # gate/up and down as two launches
+    # route + dispatch through moe_route_permute (one launch for small batches); then
+    if split:  # gate/up, down and combine as separate calls (gate/up timed on its own)
         names = ["route+permute", "gate_up", "down", "combine"]
-        parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.swiglu(stream),
+        parts = [lambda: L.route_permute(ld, xd, stream), lambda: L.swiglu(stream),
                  lambda: L.down(stream), lambda: L.combine(stream)]
-    else:  # gate/up and down in one launch (moe_grouped_ffn)
-        names = ["route+permute", "gate_up+down", "combine"]
-        parts = [lambda: (L.route(ld, stream), L.permute(xd, stream)), lambda: L.ffn(stream),
-                 lambda: L.combine(stream)]
+    else:  # moe_ffn_combine: gate/up and down in one launch, the combine inside the split-K reduction
+        names = ["route+permute", FFN_PART]
+        parts = [lambda: L.route_permute(ld, xd, stream), lambda: L.ffn_combine(stream)]
     NP = len(parts)
     graphs = []
     for fn in parts:
@@ -464,9 +465,11 @@ def ffn_roofline(cfg, res, peaks, moe_src, split):
         dur_s = res["part_ms"]["gate_up"] * 1e-3
         kernel = "grouped_gemm_tc (gate/up + SwiGLU)"
     else:
-        algo = res["touched"] * (b13 + b2) + x_b + 2 * h_b + rows * cfg.H * (4 if cfg.gemm == "f32" else 2)
-        dur_s = res["part_ms"]["gate_up+down"] * 1e-3
-        kernel = "grouped_gemm_tc, gate/up + SwiGLU + down in one launch (+ its split-K reduction)"
+        ysz = 4 if cfg.gemm == "f32" else 2
+        algo = res["touched"] * (b13 + b2) + x_b + 2 * h_b + rows * cfg.H * ysz + cfg.T * cfg.H * ysz
+        dur_s = res["part_ms"][FFN_PART] * 1e-3
+        kernel = ("moe_ffn_combine: grouped_gemm_tc, gate/up + SwiGLU + down in one launch, then the split-K "
+                  "reduction with the combine")
     achieved = algo / dur_s / 1e9
     traffic = TRAFFIC.get("%s:%s:%s" % (cfg.name, "split" if split else "ffn", moe_src))
     return {"bound": "hbm", "kernel": kernel, "achieved": round(achieved, 1),
@@ -487,7 +490,7 @@ def tensor_roofline(cfg, res, peaks, split):
     if split:
         flops, dur = f13, res["part_ms"]["gate_up"] * 1e-3
     else:
-        flops, dur = f13 + f2, res["part_ms"]["gate_up+down"] * 1e-3
+        flops, dur = f13 + f2, res["part_ms"][FFN_PART] * 1e-3
     if cfg.gemm == "f32":
         return None
     peak = bf16_sus * (2.0 if cfg.gemm == "e4m3" else 1.0)
@@ -567,7 +570,7 @@ def kernel_rooflines(cfg, res, peaks, split):
         h_b += rows * (cfg.I // 128) * 4
     y_b = rows * cfg.H * (4 if cfg.gemm == "f32" else 2)
     parts = {"gate_up": res["touched"] * b13 + x_b + h_b, "down": res["touched"] * b2 + h_b + y_b,
-             "gate_up+down": res["touched"] * (b13 + b2) + x_b + 2 * h_b + y_b}
+             FFN_PART: res["touched"] * (b13 + b2) + x_b + 2 * h_b + y_b + cfg.T * cfg.H * (4 if cfg.gemm == "f32" else 2)}
     out = {}
     for name, algo in parts.items():
         if name in res["part_ms"]:

@@ -295,6 +295,38 @@ moe_status moe_grouped_ffn(const moe_problem* p, const void* xg, const float* xg
 moe_status moe_combine(const moe_problem* p, const void* yg, const int32_t* row_of, const float* w, void* out,
                        moe_stream_t stream);
 
+/* Steps 1 and 2 in one call ("MoE inference and expert parallelism", routing
+ * section and forward-pass section: fused_topk followed by the dispatch).
+ * Same arguments, outputs and numerics as moe_route_topk followed by
+ * moe_permute (ids and w are written and bit-identical to moe_route_topk's).
+ * Batches of at most 256 records (T*K <= 256) without a replica map and with
+ * E <= 256 run as one launch: every CTA chooses the experts of all tokens
+ * (one warp per token, the router's own per-token code) and derives the layout
+ * from them in shared memory; other batches run the two calls' kernels back
+ * to back.  workspace: moe_workspace_bytes(p) bytes. */
+moe_status moe_route_permute(const moe_problem* p, const float* logits, const void* x, const int32_t* phys_to_log,
+                             int32_t* ids, float* w, int32_t* masked_m, int32_t* offsets, int32_t* row_of,
+                             int32_t* src_of, void* xg, float* xg_scales, int32_t* err_flag, void* workspace,
+                             size_t workspace_bytes, moe_stream_t stream);
+
+/* Steps 3, 4 and 5 in one call ("MoE inference and expert parallelism",
+ * routing section: fused MoE runs the grouped GEMMs, the activation and
+ * moe_sum as one unit of work).  Same arguments and numerics as
+ * moe_grouped_swiglu_gemm, moe_grouped_down_gemm and moe_combine in that order
+ * (row_of and w as written by moe_permute and the router; hg, hg_scales and
+ * yg are written as by those calls; out is bit-identical to moe_combine's).
+ * bf16 experts run both GEMMs in one launch (as moe_grouped_ffn); FP8 / FP4
+ * experts in two.  When the down GEMM is split along K (decode-sized slots),
+ * the combine runs inside the split-K reduction: each record's row is
+ * reduced over the splits and enters its token's k-order sum in the same
+ * kernel; otherwise the combine kernel follows the down GEMM.
+ * workspace: moe_workspace_bytes(p) bytes. */
+moe_status moe_ffn_combine(const moe_problem* p, const void* xg, const float* xg_scales, const void* w13,
+                           const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
+                           const int32_t* offsets, const int32_t* row_of, const float* w, void* hg, float* hg_scales,
+                           void* yg, void* out, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream);
+
 /* EPLB load statistics ("vLLM EPLB", section 1.2: expert_load_pass and
  * expert_load_window).  Copies this pass's per-slot row counts masked_m[0..P)
  * (as written by moe_permute; the shared slot is not recorded) into row

@@ -28,6 +28,7 @@ EXPORTS = ["moe_version", "moe_status_string", "moe_grouped_rows", "moe_workspac
            "moe_gemm_tile_rows",
            "moe_route_topk", "moe_route_grouped_topk", "moe_permute", "moe_permute_no_workspace",
            "moe_grouped_swiglu_gemm", "moe_grouped_down_gemm", "moe_grouped_ffn", "moe_combine",
+           "moe_route_permute", "moe_ffn_combine",
            "moe_eplb_record", "moe_eplb_rebalance", "moe_eplb_invert", "moe_selftest_bounded_wait"]
 
 
@@ -90,6 +91,10 @@ def lib():
     L.moe_grouped_down_gemm.restype = i32
     L.moe_grouped_ffn.argtypes = [pp] + [vp] * 13 + [sz, vp]
     L.moe_grouped_ffn.restype = i32
+    L.moe_route_permute.argtypes = [pp] + [vp] * 13 + [sz, vp]
+    L.moe_route_permute.restype = i32
+    L.moe_ffn_combine.argtypes = [pp] + [vp] * 16 + [sz, vp]
+    L.moe_ffn_combine.restype = i32
     L.moe_combine.argtypes = [pp, vp, vp, vp, vp, vp]
     L.moe_combine.restype = i32
     L.moe_eplb_record.argtypes = [pp, vp, i64, i32, vp, vp]
@@ -200,6 +205,24 @@ def moe_grouped_ffn(p: Problem, xg, xg_scales, w13, w13_scales, w2, w2_scales, m
     _check(lib().moe_grouped_ffn(ctypes.byref(p), _ptr(xg), _ptr(xg_scales), _ptr(w13), _ptr(w13_scales), _ptr(w2),
                                  _ptr(w2_scales), _ptr(masked_m), _ptr(offsets), _ptr(hg), _ptr(hg_scales), _ptr(yg),
                                  _ptr(err_flag), _ptr(workspace), nbytes, _stream(stream)), "moe_grouped_ffn")
+
+
+def moe_route_permute(p: Problem, logits, x, phys_to_log, ids, w, masked_m, offsets, row_of, src_of, xg, xg_scales,
+                      err_flag, workspace, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().moe_route_permute(ctypes.byref(p), _ptr(logits), _ptr(x), _ptr(phys_to_log), _ptr(ids), _ptr(w),
+                                   _ptr(masked_m), _ptr(offsets), _ptr(row_of), _ptr(src_of), _ptr(xg),
+                                   _ptr(xg_scales), _ptr(err_flag), _ptr(workspace), nbytes, _stream(stream)),
+           "moe_route_permute")
+
+
+def moe_ffn_combine(p: Problem, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, row_of, w, hg,
+                    hg_scales, yg, out, err_flag, workspace, stream=None) -> None:
+    nbytes = workspace.numel() * workspace.element_size() if workspace is not None else 0
+    _check(lib().moe_ffn_combine(ctypes.byref(p), _ptr(xg), _ptr(xg_scales), _ptr(w13), _ptr(w13_scales), _ptr(w2),
+                                 _ptr(w2_scales), _ptr(masked_m), _ptr(offsets), _ptr(row_of), _ptr(w), _ptr(hg),
+                                 _ptr(hg_scales), _ptr(yg), _ptr(out), _ptr(err_flag), _ptr(workspace), nbytes,
+                                 _stream(stream)), "moe_ffn_combine")
 
 
 def moe_combine(p: Problem, yg, row_of, w, out, stream=None) -> None:

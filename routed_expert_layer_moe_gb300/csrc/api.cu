@@ -245,6 +245,56 @@ moe_status moe_grouped_ffn(const moe_problem* p, const void* xg, const float* xg
                                      hg_scales, yg, err_flag, workspace, (cudaStream_t)stream));
 }
 
+moe_status moe_route_permute(const moe_problem* p, const float* logits, const void* x, const int32_t* phys_to_log,
+                             int32_t* ids, float* w, int32_t* masked_m, int32_t* offsets, int32_t* row_of,
+                             int32_t* src_of, void* xg, float* xg_scales, int32_t* err_flag, void* workspace,
+                             size_t workspace_bytes, moe_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return (moe_status)r;
+  if (!masked_m || !offsets || !err_flag || !workspace) return MOE_ERR_INVALID;
+  if (p->T > 0 && (!logits || !ids || !w || !x || !row_of || !src_of || !xg)) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && p->T > 0 && !xg_scales) return MOE_ERR_INVALID;
+  if (!phys_to_log && p->P != p->E) return MOE_ERR_INVALID;
+  if (p->T > 0 && (!aligned16(x) || !aligned16(xg))) return MOE_ERR_UNSUPPORTED;
+  if (workspace_bytes < ws_bytes(*p)) return MOE_ERR_WORKSPACE;
+  const cudaStream_t st = (cudaStream_t)stream;
+  if (route_permute_one_launch(*p, phys_to_log))
+    return launched(launch_route_permute_small(*p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg,
+                                               xg_scales, err_flag, st));
+  r = launch_route(*p, logits, ids, w, st);
+  if (r) return (moe_status)r;
+  return launched(launch_permute(*p, ids, x, phys_to_log, masked_m, offsets, row_of, src_of, xg, xg_scales, err_flag,
+                                 workspace, st));
+}
+
+moe_status moe_ffn_combine(const moe_problem* p, const void* xg, const float* xg_scales, const void* w13,
+                           const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
+                           const int32_t* offsets, const int32_t* row_of, const float* w, void* hg, float* hg_scales,
+                           void* yg, void* out, int32_t* err_flag, void* workspace, size_t workspace_bytes,
+                           moe_stream_t stream) {
+  int r = check_problem(p);
+  if (r) return (moe_status)r;
+  if (!xg || !w13 || !w2 || !masked_m || !offsets || !hg || !yg || !err_flag) return MOE_ERR_INVALID;
+  if (p->T > 0 && (!row_of || !w || !out)) return MOE_ERR_INVALID;
+  if (fp8_acts(*p) && (!xg_scales || !w13_scales || !w2_scales || !hg_scales)) return MOE_ERR_INVALID;
+  if (!aligned16(xg) || !aligned16(w13) || !aligned16(w2) || !aligned16(hg) || !aligned16(yg) ||
+      (p->T > 0 && !aligned16(out)))
+    return MOE_ERR_UNSUPPORTED;
+  if (p->wt == MOE_E2M1 && ((reinterpret_cast<uintptr_t>(w13) | reinterpret_cast<uintptr_t>(w2)) & 31u))
+    return MOE_ERR_UNSUPPORTED;
+  if (workspace_bytes < ws_bytes(*p) || (ws_bytes(*p) > 0 && !workspace)) return MOE_ERR_WORKSPACE;
+  const cudaStream_t st = (cudaStream_t)stream;
+  const CombineArgs comb{row_of, w, out};
+  if (p->wt == MOE_BF16)  // one launch for both GEMMs
+    return launched(launch_grouped_ffn(*p, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg,
+                                       hg_scales, yg, err_flag, workspace, st, &comb));
+  r = launch_gemm(*p, MODE_SWIGLU, xg, xg_scales, w13, w13_scales, masked_m, offsets, hg, hg_scales, err_flag,
+                  workspace, st);
+  if (r) return (moe_status)r;
+  return launched(launch_gemm(*p, MODE_DOWN, hg, hg_scales, w2, w2_scales, masked_m, offsets, yg, nullptr, err_flag,
+                              workspace, st, &comb));
+}
+
 moe_status moe_combine(const moe_problem* p, const void* yg, const int32_t* row_of, const float* w, void* out,
                        moe_stream_t stream) {
   int r = check_problem(p);

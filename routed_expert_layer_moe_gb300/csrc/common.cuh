@@ -27,6 +27,14 @@ const DeviceInfo& device_info();  // of the current device, cached
 CUresult encode_tensor_map(CUtensorMap* map, CUtensorMapDataType dtype, uint64_t inner, uint64_t outer,
                            uint64_t row_bytes, uint32_t box_inner, uint32_t box_outer, const void* base);
 
+// The combine's arguments, when a GEMM call also runs step 5 (fused into its split-K reduction,
+// or after it).
+struct CombineArgs {
+  const int32_t* row_of;
+  const float* w;
+  void* out;
+};
+
 // Per-call launchers (each returns a moe_status).
 int launch_route(const moe_problem& p, const float* logits, int32_t* ids, float* w, cudaStream_t st);
 int launch_route_grouped(const moe_problem& p, const float* logits, const float* bias, int n_group, int topk_group,
@@ -35,15 +43,20 @@ int launch_permute(const moe_problem& p, const int32_t* ids, const void* x, cons
                    int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg, float* xg_scales, int32_t* err,
                    void* ws, cudaStream_t st);
 size_t permute_workspace_bytes(const moe_problem& p);
+// Route + dispatch in one launch (batches of at most 256 records, no replica map, E <= 256).
+bool route_permute_one_launch(const moe_problem& p, const int32_t* p2l);
+int launch_route_permute_small(const moe_problem& p, const float* logits, const void* x, int32_t* ids, float* w,
+                               int32_t* masked_m, int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg,
+                               float* xg_scales, int32_t* err, cudaStream_t st);
 int launch_gemm(const moe_problem& p, int mode, const void* a_act, const float* a_act_scales, const void* w,
                 const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out,
-                float* out_scales, int32_t* err, void* ws, cudaStream_t st);
+                float* out_scales, int32_t* err, void* ws, cudaStream_t st, const CombineArgs* comb = nullptr);
 size_t gemm_workspace_bytes(const moe_problem& p);
 int gemm_tile_rows(const moe_problem& p, int mode);  // token rows of one MMA tile (0: CUDA-core GEMM)
 int launch_grouped_ffn(const moe_problem& p, const void* xg, const float* xg_scales, const void* w13,
                        const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
                        const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err, void* ws,
-                       cudaStream_t st);
+                       cudaStream_t st, const CombineArgs* comb = nullptr);
 int launch_eplb_record(const moe_problem& p, const int32_t* masked_m, int64_t pass, int window, int32_t* load_window,
                        cudaStream_t st);
 int launch_eplb_rebalance(const moe_problem& p, const int32_t* load_window, int window, const int32_t* p2l,

@@ -940,6 +940,81 @@ __global__ void __launch_bounds__(256) splitk_reduce_kernel(const float* __restr
   *reinterpret_cast<uint2*>(out + (size_t)row * cols + c) = o;
 }
 
+// Split-K reduction and combine in one kernel ("MoE inference and expert parallelism",
+// routing section: moe_sum weighs each token's K expert outputs by its route weights, plus
+// the shared expert with weight 1): for token t and each of its records k in order, the
+// record's row of the down GEMM is reduced over the splits exactly as splitk_reduce_kernel
+// does (fp32 adds in split order, one rounding to bf16, stored to yg), and that bf16 value
+// enters the token's fp32 sum as in combine_kernel (fmaf in k order, one rounding) -- the
+// same yg and out as the two kernels.  One CTA per (token, 1024 columns), 8 columns a thread.
+__global__ void __launch_bounds__(128) splitk_reduce_combine_kernel(
+    const float* __restrict__ part, int ksplit, long rows, int H, const int32_t* __restrict__ row_of,
+    const float* __restrict__ w, int K, int KS, __nv_bfloat16* __restrict__ yg, __nv_bfloat16* __restrict__ out) {
+  const int t = blockIdx.x;
+  const int c = (int)(blockIdx.y * blockDim.x + threadIdx.x) * 8;
+  __shared__ int rws[33];
+  __shared__ float wts[33];
+  if ((int)threadIdx.x < KS) {
+    rws[threadIdx.x] = row_of[(size_t)t * KS + threadIdx.x];
+    wts[threadIdx.x] = ((int)threadIdx.x < K) ? w[(size_t)t * K + threadIdx.x] : 1.0f;
+  }
+  __syncthreads();
+  if (c >= H) return;
+  float acc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) acc[i] = 0.0f;
+  for (int k = 0; k < KS; ++k) {
+    const int row = rws[k];
+    if (row < 0) continue;
+    float4 a0 = make_float4(0.f, 0.f, 0.f, 0.f), a1 = a0;
+    constexpr int QB = 8;
+    for (int q0 = 0; q0 < ksplit; q0 += QB) {
+      float4 v0[QB], v1[QB];
+#pragma unroll
+      for (int j = 0; j < QB; ++j) {
+        if (q0 + j < ksplit) {
+          const float* src = part + ((size_t)(q0 + j) * rows + row) * H + c;
+          v0[j] = __ldcg(reinterpret_cast<const float4*>(src));
+          v1[j] = __ldcg(reinterpret_cast<const float4*>(src + 4));
+        }
+      }
+#pragma unroll
+      for (int j = 0; j < QB; ++j) {
+        if (q0 + j < ksplit) {
+          a0.x += v0[j].x;
+          a0.y += v0[j].y;
+          a0.z += v0[j].z;
+          a0.w += v0[j].w;
+          a1.x += v1[j].x;
+          a1.y += v1[j].y;
+          a1.z += v1[j].z;
+          a1.w += v1[j].w;
+        }
+      }
+    }
+    uint4 yv;
+    yv.x = pack_bf16x2(a0.x, a0.y);
+    yv.y = pack_bf16x2(a0.z, a0.w);
+    yv.z = pack_bf16x2(a1.x, a1.y);
+    yv.w = pack_bf16x2(a1.z, a1.w);
+    *reinterpret_cast<uint4*>(yg + (size_t)row * H + c) = yv;
+    const float wk = wts[k];
+    const __nv_bfloat162* hv = reinterpret_cast<const __nv_bfloat162*>(&yv);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(hv[i]);
+      acc[2 * i] = fmaf(wk, f.x, acc[2 * i]);
+      acc[2 * i + 1] = fmaf(wk, f.y, acc[2 * i + 1]);
+    }
+  }
+  uint4 o;
+  o.x = pack_bf16x2(acc[0], acc[1]);
+  o.y = pack_bf16x2(acc[2], acc[3]);
+  o.z = pack_bf16x2(acc[4], acc[5]);
+  o.w = pack_bf16x2(acc[6], acc[7]);
+  *reinterpret_cast<uint4*>(out + (size_t)t * H + c) = o;
+}
+
 // ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
@@ -1135,8 +1210,20 @@ TcParams make_params(const moe_problem& p, const Plan& pl, const int32_t* masked
   return prm;
 }
 
+// After the down GEMM: the split-K reduction (when the GEMM was split), and the combine when
+// comb is given -- fused into the reduction, or on its own after an unsplit GEMM.
 int launch_reduce(const moe_problem& p, const Plan& pl, const Phase& f, const int32_t* masked_m,
-                  const int32_t* offsets, cudaStream_t st) {
+                  const int32_t* offsets, cudaStream_t st, const CombineArgs* comb = nullptr) {
+  if (comb && pl.ksplit > 1) {
+    if (p.T == 0) return MOE_OK;
+    const dim3 grid((unsigned)p.T, (unsigned)((p.H / 8 + 127) / 128));
+    splitk_reduce_combine_kernel<<<grid, 128, 0, st>>>(f.part, pl.ksplit, (long)grouped_rows(p), p.H, comb->row_of,
+                                                       comb->w, p.K, p.K + p.has_shared,
+                                                       static_cast<__nv_bfloat16*>(f.out),
+                                                       static_cast<__nv_bfloat16*>(comb->out));
+    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  }
+  if (comb) return launch_combine(p, f.out, comb->row_of, comb->w, comb->out, st);
   if (pl.ksplit <= 1) return MOE_OK;
   const long rows = (long)grouped_rows(p);
   const dim3 grid((unsigned)rows, (unsigned)((f.out_cols / 4 + 255) / 256));
@@ -1177,7 +1264,7 @@ int pair_clusters(size_t smem) {
 template <bool F8, int MODE, bool TM, bool PAIR = false>
 int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float* act_scales, const void* w,
               const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
-              int32_t* err, void* ws, cudaStream_t st) {
+              int32_t* err, void* ws, cudaStream_t st, const CombineArgs* comb) {
   auto kern = grouped_gemm_tc_kernel<F8, MODE, TM, PAIR>;
   int r = prepare_kernel<F8, MODE, TM, PAIR>();
   if (r) return r;
@@ -1212,7 +1299,7 @@ int launch_tc(const moe_problem& p, const Plan& pl, const void* act, const float
                                                                tB[2], tB[3], prm);
   }
   if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
-  return launch_reduce(p, pl, prm.ph[0], masked_m, offsets, st);
+  return launch_reduce(p, pl, prm.ph[0], masked_m, offsets, st, comb);
 }
 
 // Gate/up and down in one cooperative launch: every CTA works through the gate/up units and
@@ -1222,7 +1309,7 @@ template <bool F8, bool TM>
 int launch_ffn(const moe_problem& p, const Plan& pl0, const Plan& pl1, const void* xg, const float* xg_scales,
                const void* w13, const float* w13_scales, const void* w2, const float* w2_scales,
                const int32_t* masked_m, const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err,
-               void* ws, cudaStream_t st) {
+               void* ws, cudaStream_t st, const CombineArgs* comb) {
   auto kern = grouped_gemm_tc_kernel<F8, MODE_FFN, TM>;
   int r = prepare_kernel<F8, MODE_FFN, TM>();
   if (r) return r;
@@ -1251,7 +1338,7 @@ int launch_ffn(const moe_problem& p, const Plan& pl0, const Plan& pl1, const voi
   if (cudaLaunchKernelEx(&cfg, kern, tA, tB[0], tB[1], tB[2], tB[3], tA2, tC[0], tC[1], tC[2], tC[3], prm) !=
       cudaSuccess)
     return MOE_ERR_CUDA;
-  return launch_reduce(p, pl1, prm.ph[1], masked_m, offsets, st);
+  return launch_reduce(p, pl1, prm.ph[1], masked_m, offsets, st, comb);
 }
 
 // ---------------------------------------------------------------------------
@@ -1332,7 +1419,7 @@ size_t gemm_workspace_bytes(const moe_problem& p) {
 
 int launch_gemm(const moe_problem& p, int mode, const void* act, const float* act_scales, const void* w,
                 const float* w_scales, const int32_t* masked_m, const int32_t* offsets, void* out, float* out_scales,
-                int32_t* err, void* ws, cudaStream_t st) {
+                int32_t* err, void* ws, cudaStream_t st, const CombineArgs* comb) {
   const int nslots = p.P + p.has_shared;
   if (p.wt == MOE_F32) {
     const int K = (mode == MODE_SWIGLU) ? p.H : p.I;
@@ -1349,7 +1436,8 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
       grouped_gemm_f32_kernel<MODE_DOWN><<<grid, 256, 0, st>>>(
           (const float*)act, (const float*)w, masked_m, offsets, (float*)out, nslots,
           p.layout == MOE_LAYOUT_MASKED, p.M_max, rows, K, NA, out_cols, p.I);
-    return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    if (cudaGetLastError() != cudaSuccess) return MOE_ERR_CUDA;
+    return comb ? launch_combine(p, out, comb->row_of, comb->w, comb->out, st) : MOE_OK;
   }
   const DeviceInfo& di = device_info();
   const Plan pl = make_plan(p, mode, di.sm_count, di.max_smem_optin);
@@ -1357,14 +1445,14 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
   const bool f8 = fp8_acts(p);
 #define MOE_LAUNCH(F8_, MODE_, TM_)                                                                              \
   return launch_tc<F8_, MODE_, TM_>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out, out_scales, err, \
-                                    ws, st)
+                                    ws, st, comb)
   if (f8) {
     if (pl.pair) {
       if (mode == MODE_SWIGLU)
         return launch_tc<true, MODE_SWIGLU, true, true>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out,
-                                                        out_scales, err, ws, st);
+                                                        out_scales, err, ws, st, comb);
       return launch_tc<true, MODE_DOWN, true, true>(p, pl, act, act_scales, w, w_scales, masked_m, offsets, out,
-                                                    out_scales, err, ws, st);
+                                                    out_scales, err, ws, st, comb);
     }
     if (mode == MODE_SWIGLU) MOE_LAUNCH(true, MODE_SWIGLU, true);
     MOE_LAUNCH(true, MODE_DOWN, true);
@@ -1381,11 +1469,11 @@ int launch_gemm(const moe_problem& p, int mode, const void* act, const float* ac
 int launch_grouped_ffn(const moe_problem& p, const void* xg, const float* xg_scales, const void* w13,
                        const float* w13_scales, const void* w2, const float* w2_scales, const int32_t* masked_m,
                        const int32_t* offsets, void* hg, float* hg_scales, void* yg, int32_t* err, void* ws,
-                       cudaStream_t st) {
+                       cudaStream_t st, const CombineArgs* comb) {
   if (p.wt == MOE_F32) {  // CUDA-core path: the two GEMMs one after the other
     int r = launch_gemm(p, MODE_SWIGLU, xg, nullptr, w13, nullptr, masked_m, offsets, hg, nullptr, err, ws, st);
     if (r) return r;
-    return launch_gemm(p, MODE_DOWN, hg, nullptr, w2, nullptr, masked_m, offsets, yg, nullptr, err, ws, st);
+    return launch_gemm(p, MODE_DOWN, hg, nullptr, w2, nullptr, masked_m, offsets, yg, nullptr, err, ws, st, comb);
   }
   const DeviceInfo& di = device_info();
   const Plan pl0 = make_plan(p, MODE_SWIGLU, di.sm_count, di.max_smem_optin, 2);
@@ -1393,12 +1481,12 @@ int launch_grouped_ffn(const moe_problem& p, const void* xg, const float* xg_sca
   if (pl0.stages == 0 || pl1.stages != pl0.stages || pl1.smem != pl0.smem) return MOE_ERR_UNSUPPORTED;
   if (fp8_acts(p))
     return launch_ffn<true, true>(p, pl0, pl1, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg,
-                                  hg_scales, yg, err, ws, st);
+                                  hg_scales, yg, err, ws, st, comb);
   if (pl0.tm)
     return launch_ffn<false, true>(p, pl0, pl1, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets,
-                                   hg, hg_scales, yg, err, ws, st);
+                                   hg, hg_scales, yg, err, ws, st, comb);
   return launch_ffn<false, false>(p, pl0, pl1, xg, xg_scales, w13, w13_scales, w2, w2_scales, masked_m, offsets, hg,
-                                  hg_scales, yg, err, ws, st);
+                                  hg_scales, yg, err, ws, st, comb);
 }
 
 }  // namespace moe

@@ -26,6 +26,7 @@
 #include <algorithm>
 
 #include "common.cuh"
+#include "route_select.cuh"
 
 namespace moe {
 namespace {
@@ -434,15 +435,21 @@ __global__ void __launch_bounds__(256) scatter_kernel(const TX* __restrict__ x, 
 // from lower tokens in each of its slots -- then copies its part of the token.  The results
 // are those of mark + scan + scatter (rows of a slot in ascending token order); CTA (0, 0)
 // writes masked_m, offsets and the flags.
+// RPER > 0 (route + dispatch in one launch, E <= 32 * RPER): the ids are not read but chosen
+// in the CTA from the logits, one warp per token, by the router's own per-token code (the
+// same ids and weights as the router kernel); the CTAs of column split 0 write their token's
+// ids and weights.
 constexpr int kOneLaunchRecords = 256;  // T*K
 constexpr int kSlotsMax = 1024;         // P+S
 constexpr int kSmallThreads = 256;
 
-template <typename TX, bool QUANT>
+template <typename TX, bool QUANT, int RPER = 0>
 __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
     const int32_t* __restrict__ ids, const TX* __restrict__ x, int H, int T, int K, int E, int P, int S, int masked,
     int M_max, int32_t* __restrict__ masked_m, int32_t* __restrict__ offsets, int32_t* __restrict__ row_of,
-    int32_t* __restrict__ src_of, void* __restrict__ xg, float* __restrict__ xg_scales, int32_t* err) {
+    int32_t* __restrict__ src_of, void* __restrict__ xg, float* __restrict__ xg_scales, int32_t* err,
+    const float* __restrict__ logits = nullptr, int32_t* __restrict__ ids_out = nullptr,
+    float* __restrict__ w_out = nullptr) {
   __shared__ int32_t rec[kOneLaunchRecords];  // the ids
   __shared__ int32_t cnt[kSlotsMax];          // rows per slot
   __shared__ int32_t below[kSlotsMax];        // rows per slot from tokens before this CTA's token
@@ -456,7 +463,32 @@ __global__ void __launch_bounds__(kSmallThreads) permute_small_kernel(
     cnt[s] = (s == P) ? T : 0;  // slot P (when present) is the shared expert: one row per token
     below[s] = (s == P) ? t : 0;
   }
-  if ((int)threadIdx.x < n) rec[threadIdx.x] = ids[threadIdx.x];
+  if constexpr (RPER > 0) {
+    // the next token's logits are requested before this token's selection
+    float v[RPER], vn[RPER];
+    uint32_t avail = 0, availn = 0;
+    if (warp < T) avail = route_load<RPER>(logits + (size_t)warp * E, E, lane, v);
+    for (int tt = warp; tt < T; tt += kSmallThreads / 32) {
+      const int tn = tt + kSmallThreads / 32;
+      if (tn < T) availn = route_load<RPER>(logits + (size_t)tn * E, E, lane, vn);
+      int id;
+      float val;
+      route_select<RPER>(v, avail, K, lane, id, val);
+      const float wt = route_weight(val, K, lane);
+      if (lane < K) {
+        rec[tt * K + lane] = id;
+        if (tt == t && blockIdx.y == 0) {
+          ids_out[(size_t)tt * K + lane] = id;
+          w_out[(size_t)tt * K + lane] = wt;
+        }
+      }
+#pragma unroll
+      for (int i = 0; i < RPER; ++i) v[i] = vn[i];
+      avail = availn;
+    }
+  } else {
+    if ((int)threadIdx.x < n) rec[threadIdx.x] = ids[threadIdx.x];
+  }
   __syncthreads();
   int flags = 0;
   int sl = -1;
@@ -745,7 +777,51 @@ void launch_small(const moe_problem& p, const int32_t* ids, const void* x, const
   }
 }
 
+template <typename TX, bool QUANT, int RPER>
+void launch_route_small(const moe_problem& p, const float* logits, const void* x, int32_t* ids, float* w,
+                        int32_t* masked_m, int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg,
+                        float* xg_scales, int32_t* err, cudaStream_t st) {
+  const dim3 grid(p.T, copy_splits(p, (int)sizeof(TX)));
+  permute_small_kernel<TX, QUANT, RPER><<<grid, kSmallThreads, 0, st>>>(
+      nullptr, static_cast<const TX*>(x), p.H, p.T, p.K, p.E, p.P, p.has_shared, p.layout == MOE_LAYOUT_MASKED,
+      p.M_max, masked_m, offsets, row_of, src_of, xg, xg_scales, err, logits, ids, w);
+}
+
+template <typename TX, bool QUANT>
+void launch_route_small_per(const moe_problem& p, const float* logits, const void* x, int32_t* ids, float* w,
+                            int32_t* masked_m, int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg,
+                            float* xg_scales, int32_t* err, cudaStream_t st) {
+  const int per = (p.E + 31) / 32;
+  if (per <= 1)
+    launch_route_small<TX, QUANT, 1>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg, xg_scales, err, st);
+  else if (per <= 2)
+    launch_route_small<TX, QUANT, 2>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg, xg_scales, err, st);
+  else if (per <= 4)
+    launch_route_small<TX, QUANT, 4>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg, xg_scales, err, st);
+  else
+    launch_route_small<TX, QUANT, 8>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg, xg_scales, err, st);
+}
+
 }  // namespace
+
+bool route_permute_one_launch(const moe_problem& p, const int32_t* p2l) {
+  return p.T > 0 && (int64_t)p.T * p.K <= kOneLaunchRecords && !p2l && p.E <= 256;
+}
+
+int launch_route_permute_small(const moe_problem& p, const float* logits, const void* x, int32_t* ids, float* w,
+                               int32_t* masked_m, int32_t* offsets, int32_t* row_of, int32_t* src_of, void* xg,
+                               float* xg_scales, int32_t* err, cudaStream_t st) {
+  if (fp8_acts(p))
+    launch_route_small_per<__nv_bfloat16, true>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg,
+                                                xg_scales, err, st);
+  else if (p.wt == MOE_BF16)
+    launch_route_small_per<__nv_bfloat16, false>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg,
+                                                 xg_scales, err, st);
+  else
+    launch_route_small_per<float, false>(p, logits, x, ids, w, masked_m, offsets, row_of, src_of, xg, xg_scales,
+                                         err, st);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
 
 size_t permute_workspace_bytes(const moe_problem& p) {
   size_t total = 0;

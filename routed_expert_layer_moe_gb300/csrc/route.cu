@@ -5,7 +5,7 @@
 // the fp32 logits themselves (softmax is strictly increasing, so the chosen
 // set is the same and no rounding of exp can create new ties); ties go to the
 // lower expert index.  Weights: exp(l_k - l_max) / sum over the chosen K.
-#include "common.cuh"
+#include "route_select.cuh"
 
 namespace moe {
 namespace {
@@ -47,13 +47,7 @@ __global__ void __launch_bounds__(256, CAND ? (PER >= 32 ? 2 : 4) : 1) route_top
   if (t >= T) return;
   const float* l = logits + (size_t)t * E;
   float v[PER];
-  uint32_t avail = 0;  // bit i: expert lane + 32*i not yet chosen
-#pragma unroll
-  for (int i = 0; i < PER; ++i) {
-    const int e = lane + 32 * i;
-    v[i] = (e < E) ? __ldg(l + e) : -INFINITY;
-    if (e < E) avail |= 1u << i;
-  }
+  uint32_t avail = route_load<PER>(l, E, lane, v);  // bit i: expert lane + 32*i not yet chosen
   if constexpr (CAND) {
     static_assert(PER >= 4, "every lane must hold an expert");
     // Candidates first: tau, the K-th of the 32 lane maxima in the order above, has K
@@ -111,43 +105,13 @@ __global__ void __launch_bounds__(256, CAND ? (PER >= 32 ? 2 : 4) : 1) route_top
       return;
     }
   }
-  int my_id = 0;
-  float my_val = 0.0f;
-  for (int k = 0; k < K; ++k) {
-    // best remaining candidate of this lane: largest value, lowest index on ties
-    float bv = -INFINITY;
-    int be = 0x7fffffff;
-#pragma unroll
-    for (int i = 0; i < PER; ++i) {
-      if ((avail >> i) & 1u) {
-        if (be == 0x7fffffff || v[i] > bv) {
-          bv = v[i];
-          be = lane + 32 * i;
-        }
-      }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) {
-      const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-      const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-      if (ov > bv || (ov == bv && oe < be)) {
-        bv = ov;
-        be = oe;
-      }
-    }
-    if ((be & 31) == lane) avail &= ~(1u << (be >> 5));
-    if (lane == k) {
-      my_id = be;
-      my_val = bv;
-    }
-  }
-  const float lmax = __shfl_sync(0xffffffffu, my_val, 0);
-  const float ex = (lane < K) ? expf(my_val - lmax) : 0.0f;
-  float sum = 0.0f;
-  for (int k = 0; k < K; ++k) sum += __shfl_sync(0xffffffffu, ex, k);  // fixed order k = 0..K-1
+  int my_id;
+  float my_val;
+  route_select<PER>(v, avail, K, lane, my_id, my_val);
+  const float wt = route_weight(my_val, K, lane);
   if (lane < K) {
     ids[(size_t)t * K + lane] = my_id;
-    w[(size_t)t * K + lane] = ex / sum;
+    w[(size_t)t * K + lane] = wt;
   }
 }
 

@@ -82,15 +82,27 @@ class MoeLayer:
     def combine(self, stream=None):
         L.moe_combine(self.p, self.yg, self.row_of, self.w, self.out, stream)
 
+    def route_permute(self, logits, x, stream=None):
+        """route() + permute() in one call (moe_route_permute; one launch for small batches)."""
+        L.moe_route_permute(self.p, logits, x, self.p2l, self.ids, self.w, self.masked_m, self.offsets, self.row_of,
+                            self.src_of, self.xg, self.xg_s, self.err, self.ws, stream)
+
+    def ffn_combine(self, stream=None):
+        """gate/up, down and combine in one call (moe_ffn_combine); same outputs as swiglu() + down() + combine()."""
+        L.moe_ffn_combine(self.p, self.xg, self.xg_s, self.w13, self.w13_s, self.w2, self.w2_s, self.masked_m,
+                          self.offsets, self.row_of, self.w, self.hg, self.hg_s, self.yg, self.out, self.err, self.ws,
+                          stream)
+
     def forward(self, x, logits, stream=None, fused=False):
-        """route -> permute -> gate/up -> down -> combine; returns self.out.  fused=True runs
-        gate/up and down as one launch (ffn())."""
+        """route -> permute -> gate/up -> down -> combine; returns self.out.  fused=True makes the
+        same pass with the fused calls: route_permute() and ffn_combine()."""
+        if fused:
+            self.route_permute(logits, x, stream)
+            self.ffn_combine(stream)
+            return self.out
         self.route(logits, stream)
         self.permute(x, stream)
-        if fused:
-            self.ffn(stream)
-        else:
-            self.swiglu(stream)
-            self.down(stream)
+        self.swiglu(stream)
+        self.down(stream)
         self.combine(stream)
         return self.out

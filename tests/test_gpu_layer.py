@@ -131,3 +131,47 @@ def test_layer_full_size_sampled(name, request):
                 assert (gx[r] == q[i]).all() and (gs[r] == s[i]).all()
     del L
     torch.cuda.empty_cache()
+
+
+def run_layer(wl, fused):
+    """The whole pass through the separate calls or through moe_route_permute +
+    moe_ffn_combine; every output buffer, with padding rows of the grouped buffers set to a
+    sentinel first."""
+    L = wl.layer()
+    for t in (L.xg, L.hg):
+        t.zero_()
+    L.yg.fill_(-3.0)
+    L.forward(to_dev(wl.x), to_dev(wl.logits), fused=fused)
+    torch.cuda.synchronize()
+    assert int(to_host(L.err)[0]) == 0
+    outs = {n: to_host(getattr(L, n))
+            for n in ("ids", "w", "masked_m", "offsets", "row_of", "src_of", "xg", "hg", "yg", "out")}
+    for n in ("xg_s", "hg_s"):
+        if getattr(L, n) is not None:
+            outs[n] = to_host(getattr(L, n))
+    return outs, L
+
+
+@pytest.mark.parametrize("name", list(SMALL) + ["bf16_split_k", "e4m3_t1"])
+def test_fused_calls_bit_identical(name):
+    """moe_route_permute and moe_ffn_combine give the separate calls' outputs bit for bit: ids,
+    weights, layout, the grouped buffers' valid rows (xg, hg, yg and scales) and the layer
+    output -- through the one-launch route + dispatch (small batches without a map), its
+    two-kernel fallback (replica map), the combine fused into the split-K reduction and the
+    combine after an unsplit down GEMM.  The output is also within tolerance of the oracle."""
+    # I = 1024: enough K blocks for the down GEMM of a 4-token batch to be split along K
+    extra = {"bf16_split_k": SMALL["bf16_masked"].replace(name="bf16_split_k", T=4, I=1024, M_max=4),
+             "e4m3_t1": SMALL["e4m3_masked_shared"].replace(name="e4m3_t1", T=1, M_max=1)}
+    cfg = extra.get(name) or SMALL[name]
+    wl = Workload(cfg)
+    sep, _ = run_layer(wl, False)
+    fus, L = run_layer(wl, True)
+    valid = sep["src_of"] >= 0
+    for n in ("ids", "w", "masked_m", "offsets", "row_of", "src_of", "out"):
+        assert (fus[n].view(np.uint8) == sep[n].view(np.uint8)).all(), n
+    for n in ("xg", "hg", "yg", "xg_s", "hg_s"):
+        if n in sep:
+            assert (fus[n][valid] == sep[n][valid]).all(), n
+    assert (real(fus["yg"][~valid], cfg.y_dtype) == -3.0).all()
+    ref, exact = oracle.layer(cfg, wl.x, wl.logits, wl.w13, wl.w13_s, wl.w2, wl.w2_s)
+    assert rel_err(real(fus["out"], cfg.out), exact) <= TOL[cfg.gemm]
