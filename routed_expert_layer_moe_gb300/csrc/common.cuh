@@ -433,6 +433,68 @@ __device__ __forceinline__ void tmem_wait_ld32(uint32_t (&r)[32]) {
       : "memory");
 }
 
+// Two 32-lane x 32-column fp32 loads from tensor memory (32 columns at ta, 32 at tb), waited for
+// in the same statement, as 32 packed pairs (r[i] = columns 2i, 2i+1 of ta for i < 16, of tb for
+// i >= 16; the lower column in the low word): operands of fma.rn.f32x2 that need no moves.
+__device__ __forceinline__ void tmem_ld32x2_pairs(uint32_t ta, uint32_t tb, uint64_t (&r)[32]) {
+  asm volatile(
+      "{\n"
+      "  .reg .b32 t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31, t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63;\n"
+      "  tcgen05.ld.sync.aligned.32x32b.x32.b32 {t0, t1, t2, t3, t4, t5, t6, t7, t8, t9, t10, t11, t12, t13, t14, t15, t16, t17, t18, t19, t20, t21, t22, t23, t24, t25, t26, t27, t28, t29, t30, t31}, [%32];\n"
+      "  tcgen05.ld.sync.aligned.32x32b.x32.b32 {t32, t33, t34, t35, t36, t37, t38, t39, t40, t41, t42, t43, t44, t45, t46, t47, t48, t49, t50, t51, t52, t53, t54, t55, t56, t57, t58, t59, t60, t61, t62, t63}, [%33];\n"
+      "  tcgen05.wait::ld.sync.aligned;\n"
+      "  mov.b64 %0, {t0, t1};\n"
+      "  mov.b64 %1, {t2, t3};\n"
+      "  mov.b64 %2, {t4, t5};\n"
+      "  mov.b64 %3, {t6, t7};\n"
+      "  mov.b64 %4, {t8, t9};\n"
+      "  mov.b64 %5, {t10, t11};\n"
+      "  mov.b64 %6, {t12, t13};\n"
+      "  mov.b64 %7, {t14, t15};\n"
+      "  mov.b64 %8, {t16, t17};\n"
+      "  mov.b64 %9, {t18, t19};\n"
+      "  mov.b64 %10, {t20, t21};\n"
+      "  mov.b64 %11, {t22, t23};\n"
+      "  mov.b64 %12, {t24, t25};\n"
+      "  mov.b64 %13, {t26, t27};\n"
+      "  mov.b64 %14, {t28, t29};\n"
+      "  mov.b64 %15, {t30, t31};\n"
+      "  mov.b64 %16, {t32, t33};\n"
+      "  mov.b64 %17, {t34, t35};\n"
+      "  mov.b64 %18, {t36, t37};\n"
+      "  mov.b64 %19, {t38, t39};\n"
+      "  mov.b64 %20, {t40, t41};\n"
+      "  mov.b64 %21, {t42, t43};\n"
+      "  mov.b64 %22, {t44, t45};\n"
+      "  mov.b64 %23, {t46, t47};\n"
+      "  mov.b64 %24, {t48, t49};\n"
+      "  mov.b64 %25, {t50, t51};\n"
+      "  mov.b64 %26, {t52, t53};\n"
+      "  mov.b64 %27, {t54, t55};\n"
+      "  mov.b64 %28, {t56, t57};\n"
+      "  mov.b64 %29, {t58, t59};\n"
+      "  mov.b64 %30, {t60, t61};\n"
+      "  mov.b64 %31, {t62, t63};\n"
+      "}\n"
+      : "=l"(r[0]), "=l"(r[1]), "=l"(r[2]), "=l"(r[3]), "=l"(r[4]), "=l"(r[5]), "=l"(r[6]), "=l"(r[7]), "=l"(r[8]), "=l"(r[9]), "=l"(r[10]), "=l"(r[11]), "=l"(r[12]), "=l"(r[13]), "=l"(r[14]), "=l"(r[15]), "=l"(r[16]), "=l"(r[17]), "=l"(r[18]), "=l"(r[19]), "=l"(r[20]), "=l"(r[21]), "=l"(r[22]), "=l"(r[23]), "=l"(r[24]), "=l"(r[25]), "=l"(r[26]), "=l"(r[27]), "=l"(r[28]), "=l"(r[29]), "=l"(r[30]), "=l"(r[31])
+      : "r"(ta), "r"(tb)
+      : "memory");
+}
+
+// a[i] += r[i] * (s, s) for n packed pairs (two fmaf roundings each).
+template <int N>
+__device__ __forceinline__ void fma2_pairs(uint64_t* a, const uint64_t* r, uint64_t s2) {
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a[i]) : "l"(r[i]), "l"(s2));
+}
+
+// (s, s) as one packed pair.
+__device__ __forceinline__ uint64_t pair_of(float s) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
+  return r;
+}
+
 // a[o .. o+31] += r[0..31] * s, as sixteen packed fp32x2 multiply-adds (two fmaf roundings each).
 __device__ __forceinline__ void fma2_chunk(float* a, const uint32_t (&r)[32], float s) {
   const float2 sv = make_float2(s, s);

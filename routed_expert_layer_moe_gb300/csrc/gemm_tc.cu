@@ -694,6 +694,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
 
       if constexpr (F8) {
+        // SM pairs: the fp32 accumulators as packed pairs (accp0[i] = columns c_lo + 2i, 2i+1 of
+        // tile 0), unpacked into acc0 / acc1 after the K loop
+        uint64_t accp0[32], accp1[32];
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          accp0[i] = 0;
+          accp1[i] = 0;
+        }
         for (int k = 0; k < nkb; ++k) {
           const int j = k % SG;  // K block within its scale group (groups restart with each unit)
           const uint32_t gh = g_it & 1u;  // half of the scale ring
@@ -709,32 +717,52 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           tc_fence_after_sync();
           const int slot = (int)gh * SG + j;
           const float xs = sx[slot * BN + lrow];
-          const float p0 = sw[slot * 2] * xs, p1 = sw[slot * 2 + 1] * xs;
-          // four 32-column chunks (tile 0 cols c_lo.., tile 1 cols c_lo.., tile 0 cols c_lo+32..,
-          // tile 1 cols c_lo+32..), each load issued before the multiply-adds of the previous
-          // chunk so that its latency hides behind them
-          uint32_t ra[32], rb[32];
-          const uint32_t c0 = t_lane + b * 256u + (uint32_t)c_lo;
-          tmem_ld32(c0, ra);
-          tmem_wait_ld32(ra);
-          tmem_ld32(c0 + 128u, rb);
-          fma2_chunk(acc0, ra, p0);
-          tmem_wait_ld32(rb);
-          tmem_ld32(c0 + 32u, ra);
-          fma2_chunk(acc1, rb, p1);
-          tmem_wait_ld32(ra);
-          tmem_ld32(c0 + 160u, rb);
-          fma2_chunk(acc0 + 32, ra, p0);
-          tmem_wait_ld32(rb);
-          // the buffer is read: hand it back before the last multiply-adds
-          tc_fence_before_sync();
-          if (PAIR && !leader) {  // to the leader's MMA thread, which waits on its own barrier
-            __syncwarp();
-            if (lane == 0) mbar_arrive_remote(mapa_shared(&tempty[b], 0));
+          const float s0 = sw[slot * 2] * xs, s1 = sw[slot * 2 + 1] * xs;
+          if constexpr (PAIR) {
+            // SM pairs: two steps of 64 columns (tile 0 and tile 1, columns c_lo.. then c_lo+32..),
+            // loaded as packed pairs and added with fp32x2 multiply-adds on paired accumulators;
+            // the buffer is handed back once the second step is loaded, before its multiply-adds
+            const uint64_t p0 = pair_of(s0), p1 = pair_of(s1);
+            const uint32_t c0 = t_lane + b * 256u + (uint32_t)c_lo;
+#pragma unroll
+            for (int pr = 0; pr < 2; ++pr) {
+              uint64_t v[32];
+              tmem_ld32x2_pairs(c0 + (uint32_t)(pr * 32), c0 + 128u + (uint32_t)(pr * 32), v);
+              if (pr == 1) {
+                tc_fence_before_sync();
+                if (!leader) {  // to the leader's MMA thread, which waits on its own barrier
+                  __syncwarp();
+                  if (lane == 0) mbar_arrive_remote(mapa_shared(&tempty[b], 0));
+                } else {
+                  warp_arrive(&tempty[b]);
+                }
+              }
+              fma2_pairs<16>(accp0 + pr * 16, v, p0);
+              fma2_pairs<16>(accp1 + pr * 16, v + 16, p1);
+            }
           } else {
+            const float p0 = s0, p1 = s1;
+            // one CTA: four 32-column chunks (tile 0 cols c_lo.., tile 1 cols c_lo.., tile 0 cols
+            // c_lo+32.., tile 1 cols c_lo+32..), each load issued before the multiply-adds of the previous
+            // chunk so that its latency hides behind them
+            uint32_t ra[32], rb[32];
+            const uint32_t c0 = t_lane + b * 256u + (uint32_t)c_lo;
+            tmem_ld32(c0, ra);
+            tmem_wait_ld32(ra);
+            tmem_ld32(c0 + 128u, rb);
+            fma2_chunk(acc0, ra, p0);
+            tmem_wait_ld32(rb);
+            tmem_ld32(c0 + 32u, ra);
+            fma2_chunk(acc1, rb, p1);
+            tmem_wait_ld32(ra);
+            tmem_ld32(c0 + 160u, rb);
+            fma2_chunk(acc0 + 32, ra, p0);
+            tmem_wait_ld32(rb);
+            // the buffer is read: hand it back before the last multiply-adds
+            tc_fence_before_sync();
             warp_arrive(&tempty[b]);
+            fma2_chunk(acc1 + 32, rb, p1);
           }
-          fma2_chunk(acc1 + 32, rb, p1);
           if (j == SG - 1 || k == nkb - 1) {  // the group's scales are no longer read
             warp_arrive(&gempty[gh]);
             ++g_it;
@@ -742,6 +770,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++acc_it;
         }
         if (!ok) break;
+        if constexpr (PAIR) {
+#pragma unroll
+        for (int i = 0; i < 32; ++i) {
+          acc0[2 * i] = __uint_as_float((uint32_t)accp0[i]);
+          acc0[2 * i + 1] = __uint_as_float((uint32_t)(accp0[i] >> 32));
+          acc1[2 * i] = __uint_as_float((uint32_t)accp1[i]);
+          acc1[2 * i + 1] = __uint_as_float((uint32_t)(accp1[i] >> 32));
+        }
+        }
       } else {
         // BF16: the accumulator of the whole K range (or this split of it) is in tensor memory
         const uint32_t b = acc_it & 1u;
