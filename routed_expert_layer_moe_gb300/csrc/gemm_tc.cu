@@ -26,17 +26,26 @@
 //       - weight-major (BF16 decode): the weight tile is the M = 128 side and the
 //         chunk's tokens the N side, rounded up to 16 -- an expert with a few
 //         tokens streams its weights at full width and issues N = 16 MMAs.
+//   * SM pairs (FP8 / FP4 slots of prefill size, 128 rows or more on average):
+//     clusters of two CTAs, 256-row token chunks, one cta_group::2 MMA
+//     (M = 256, N = 256) per K block over both CTAs' shared memory; each CTA
+//     stages its 128 token rows and one weight tile (32 KB stages, six of them)
+//     and keeps its own rows' accumulators (see the kernel's comment).
 //   * Warp 0: TMA producer (weights with an evict-first L2 hint).  Warp 1:
 //     tensor-memory allocator and the single MMA-issuing thread.  Warps 2-3:
-//     FP8 scale loaders (the activation and weight scales of each K block into
-//     a 32-slot ring in shared memory with asynchronous 4-byte copies, up to 32
-//     K blocks ahead of the epilogue; keeping the scales out of the stages
-//     leaves room for four 48 KB stages).  Warps 4-11: epilogue, two warps per
-//     tensor-memory lane quarter.
+//     FP8 scale loaders (the activation and weight scales of up to 16 K blocks
+//     per group into one half of a two-group ring in shared memory, with
+//     asynchronous 4-byte copies; the epilogue waits and releases once per
+//     group; keeping the scales out of the stages leaves room for four 48 KB
+//     stages).  Warps 4-11: epilogue, two warps per tensor-memory lane quarter.
 //   * FP8: the MMAs of one 128-K block write one of two tensor-memory buffers;
 //     the epilogue reads it, scales it and adds it into fp32 registers while
-//     the MMA fills the other.  BF16: the whole K range accumulates in tensor
-//     memory; the two buffers alternate between units.
+//     the MMA fills the other (SM pairs: the partial sums read as packed pairs
+//     and added with fp32x2 multiply-adds on paired accumulators; one CTA: four
+//     32-column chunks, each load issued before the previous chunk's
+//     multiply-adds -- each measured the faster of the two on its kernel).
+//     BF16: the whole K range accumulates in tensor memory; the two buffers
+//     alternate between units.
 //   * MODE_FFN runs gate/up and down in one cooperative launch: the unit list
 //     is the gate/up units followed by the down units, and a down unit's token
 //     (h) tile and scales are read only after every gate/up unit of its slot
