@@ -39,6 +39,13 @@ METRIC = "MoE layer tokens/s"
 # workload, the launch form (one-launch FFN or the gate/up launch) and the hash of the
 # kernel source the capture was taken from; a changed kernel source gives no entry (null).
 TRAFFIC = {
+    # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass) on the full-size workloads: the
+    # first launch of the dominant grouped GEMM kernel in a bench process
+    "prefill:split:68655c7e51c39da2": 4820873728 + 78658816,          # gate/up, SM pairs
+    "mixtral_decode:ffn:68655c7e51c39da2": 2821667840 + 6235136,      # one-launch FFN kernel (without the reduction)
+    "dsv3_decode:split:68655c7e51c39da2": 7491763712 + 10268416,      # gate/up
+    "skew_eplb:split:68655c7e51c39da2": 2877403136 + 5199872,         # gate/up
+    "dsv4_fp4_decode:split:68655c7e51c39da2": 5073245184 + 10115328,  # gate/up
 }
 
 

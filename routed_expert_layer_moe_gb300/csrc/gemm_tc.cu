@@ -369,7 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (lane == 0) {
         tma_prefetch_map(&tmA);
         tma_prefetch_map(&tmB128);
-        if (!TM) {
+        if (!PAIR) {
           tma_prefetch_map(&tmB16);
           tma_prefetch_map(&tmB32);
           tma_prefetch_map(&tmB64);
@@ -391,8 +391,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const Unit U = locate(u, h, mode);
           const CUtensorMap* ma = h ? &tmA2 : &tmA;
           const CUtensorMap* mb = h ? &tmC128 : &tmB128;
+          // token box: the smallest of 16 / 32 / 64 / 128 rows that covers the chunk (SM pairs: 128).
+          // Token-major MMAs still read 128 rows; the rows past the box hold stale shared memory
+          // and only give accumulator rows past the chunk, which are never used or stored.
           int box = 128;
-          if (!TM) {
+          if (!PAIR) {
             if (U.nvalid <= 16) {
               mb = h ? &tmC16 : &tmB16;
               box = 16;
