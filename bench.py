@@ -41,11 +41,11 @@ METRIC = "MoE layer tokens/s"
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass) on the full-size workloads: the
     # first launch of the dominant grouped GEMM kernel in a bench process
-    "prefill:split:68655c7e51c39da2": 4820873728 + 78658816,          # gate/up, SM pairs
-    "mixtral_decode:ffn:68655c7e51c39da2": 2821667840 + 6235136,      # one-launch FFN kernel (without the reduction)
-    "dsv3_decode:split:68655c7e51c39da2": 7491763712 + 10268416,      # gate/up
-    "skew_eplb:split:68655c7e51c39da2": 2877403136 + 5199872,         # gate/up
-    "dsv4_fp4_decode:split:68655c7e51c39da2": 5073245184 + 10115328,  # gate/up
+    "prefill:split:44646a434f90d619": 4824612864 + 78791168,          # gate/up, SM pairs
+    "mixtral_decode:ffn:44646a434f90d619": 2821686528 + 5934080,      # one-launch FFN kernel (without the reduction)
+    "dsv3_decode:split:44646a434f90d619": 7491252480 + 8620800,       # gate/up
+    "skew_eplb:split:44646a434f90d619": 2876958464 + 4845312,         # gate/up
+    "dsv4_fp4_decode:split:44646a434f90d619": 5070470400 + 8520960,   # gate/up
 }
 
 

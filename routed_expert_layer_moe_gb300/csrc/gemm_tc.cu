@@ -22,7 +22,8 @@
 //       - token-major (every FP8 problem, and BF16 prefill): the 128 token rows
 //         are the MMA's M side and the gate and up tiles together one N = 256
 //         MMA; the activation scale is one value per thread, and the SwiGLU, the
-//         e4m3 re-quantisation of h and the stores are row-local;
+//         e4m3 re-quantisation of h and the stores are row-local.  FP8 chunks of
+//         at most 64 rows use M = 64 MMAs (rows 16q..16q+15 in lane quarter q);
 //       - weight-major (BF16 decode): the weight tile is the M = 128 side and the
 //         chunk's tokens the N side, rounded up to 16 -- an expert with a few
 //         tokens streams its weights at full width and issues N = 16 MMAs.
@@ -184,6 +185,13 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
   U.kb0 = U.q * f.kb_per_split;
   U.kb1 = min(f.kb_total, U.kb0 + f.kb_per_split);
   return U;
+}
+
+// Token-major FP8 / FP4 units of one CTA with at most 64 token rows (decode-sized chunks) use
+// M = 64 MMAs: half the tensor time of M = 128 for rows that would only be padding.
+template <bool F8, bool TM, bool PAIR>
+__device__ __forceinline__ bool m64_unit(const Unit& U) {
+  return F8 && TM && !PAIR && U.nvalid <= 64;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -492,7 +500,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // (token-major: the weights are the B operand, of format w_fmt)
           // (token-major FP8 / FP4: the weights are the B operand, of format w_fmt)
           const uint32_t idesc = PAIR ? (mma_idesc<F8>(2 * BM, 2 * BM) | (p.w_fmt << 10))
-                                 : TM ? (mma_idesc<F8>(BM, U.a1 ? 2 * BM : BM) | (F8 ? p.w_fmt << 10 : 0u))
+                                 : TM ? (mma_idesc<F8>(m64_unit<F8, TM, PAIR>(U) ? 64 : BM, U.a1 ? 2 * BM : BM) |
+                                         (F8 ? p.w_fmt << 10 : 0u))
                                       : mma_idesc<F8>(BM, (U.nvalid + 15) & ~15);
           uint32_t b = 0;
           if constexpr (!F8) {
@@ -692,6 +701,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t oc = (size_t)f.out_cols;
       const int nkb = U.kb1 - U.kb0;
       const bool split = f.ksplit > 1;
+      // M = 64 units (m64_unit): accumulator row r sits in lane 32 (r / 16) + r % 16, so thread
+      // (quarter q, lane l < 16) holds token row 16 q + l and lanes 16-31 of each quarter hold none
+      const bool m64 = m64_unit<F8, TM, PAIR>(U);
+      const bool evalid = !m64 || lane < 16;
+      const int erow = m64 ? (lane < 16 ? quarter * 16 + lane : 0) : lrow;  // token row of this thread
       if (h == 1) release_pending();
       // weight-major: this thread owns weight row lrow of each tile and token columns
       // [c_lo, c_lo + ncols); token-major: token row lrow and weight columns [64*half, +64)
@@ -728,7 +742,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after_sync();
           const int slot = (int)gh * SG + j;
-          const float xs = sx[slot * BN + lrow];
+          const float xs = sx[slot * BN + erow];
           const float s0 = sw[slot * 2] * xs, s1 = sw[slot * 2 + 1] * xs;
           if constexpr (PAIR) {
             // SM pairs: two steps of 64 columns (tile 0 and tile 1, columns c_lo.. then c_lo+32..),
@@ -822,8 +836,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // separate reduction kernel adds the splits in split order (no atomics, no waits)
         float* pq = f.part + (size_t)U.q * p.rows_total * oc;
         if constexpr (TM) {
-          if (lrow < U.nvalid) {
-            float* prow = pq + (size_t)(U.rowB + lrow) * oc + (size_t)U.j * f.pair_stride + c_lo;
+          if (evalid && erow < U.nvalid) {
+            float* prow = pq + (size_t)(U.rowB + erow) * oc + (size_t)U.j * f.pair_stride + c_lo;
             const bool wide = (reinterpret_cast<uintptr_t>(f.part) & 31u) == 0;  // offsets are 256-byte multiples
             store_f32x64(prow, acc0, wide);
             if (U.a1) store_f32x64(prow + BM, acc1, wide);
@@ -846,8 +860,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---- final values of this unit
       float* redp = red + (size_t)(u_it & 1u) * 512;  // maxima, double-buffered by unit parity
       if constexpr (TM) {
-        const bool row_ok = lrow < U.nvalid;
-        const size_t row = (size_t)(U.rowB + lrow);
+        const bool row_ok = evalid && erow < U.nvalid;
+        const size_t row = (size_t)(U.rowB + erow);
         if (mode == MODE_SWIGLU) {
           // rows past the chunk hold other tokens' data: no SwiGLU, no store
           if (row_ok) {

@@ -301,7 +301,10 @@ def gemm_inputs(wl):
 
 @pytest.mark.parametrize("name", NAMES)
 def test_grouped_swiglu(workloads, name):
-    wl = workloads[name]
+    check_grouped_swiglu(workloads[name])
+
+
+def check_grouped_swiglu(wl):
     cfg = wl.cfg
     lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
     hg_ref, hgs_ref = oracle.grouped_swiglu(cfg, xg, xgs, w13, w13s, lay["masked_m"], lay["offsets"])
@@ -328,7 +331,10 @@ def test_grouped_swiglu(workloads, name):
 
 @pytest.mark.parametrize("name", NAMES)
 def test_grouped_down(workloads, name):
-    wl = workloads[name]
+    check_grouped_down(workloads[name])
+
+
+def check_grouped_down(wl):
     cfg = wl.cfg
     lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
     hg, hgs = oracle.grouped_swiglu(cfg, xg, xgs, w13, w13s, lay["masked_m"], lay["offsets"])
@@ -387,6 +393,57 @@ def test_grouped_ffn_one_launch(workloads, name):
     assert (yf[valid] == ys[valid]).all()
     assert (real(yf[~valid], cfg.y_dtype) == -3.0).all()
     assert rel_err(real(yf[valid], cfg.y_dtype), real(yg_ref[valid], cfg.y_dtype)) <= TOL[cfg.gemm]
+
+
+def routing_with_counts(counts, T, K):
+    """ids [T, K] in which expert e is chosen by exactly counts[e] distinct tokens (sum(counts) =
+    T * K, every count <= T): the experts, largest count first, take consecutive runs of tokens
+    cyclically, so each token gets K distinct experts."""
+    assert sum(counts) == T * K and max(counts) <= T
+    per_token = [[] for _ in range(T)]
+    ptr = 0
+    for e in sorted(range(len(counts)), key=lambda e: -counts[e]):
+        for i in range(counts[e]):
+            per_token[(ptr + i) % T].append(e)
+        ptr += counts[e]
+    ids = np.array(per_token, np.int32)
+    assert ids.shape == (T, K) and all(len(set(r)) == K for r in per_token)
+    return ids
+
+
+# slot row counts on both sides of every token box (16 / 32 / 64 / 128 rows) and of the split of a
+# slot into two chunks (above 128 rows), plus an empty slot
+EDGE_COUNTS = [0, 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 47]
+
+
+@pytest.mark.parametrize("wq", ["e4m3", "e2m1"])
+def test_grouped_gemms_at_token_box_edges(wq):
+    """FP8 / FP4 decode-shaped GEMMs (token-major, one CTA per SM) on a layout whose slots hold
+    0, 1, 15-17, 31-33, 63-65 and 127-129 rows (and a shared expert with every token): the token
+    box of each chunk is the smallest of 16 / 32 / 64 / 128 rows covering it, and the MMA reads
+    stale shared memory past the box.  Values within tolerance of the oracle, padding rows
+    untouched, token tiles = sum over slots of ceil(rows / 128)."""
+    T, K = 192, 4
+    base = SMALL["e4m3_masked_shared"] if wq == "e4m3" else SMALL["e2m1_masked_shared"]
+    cfg = base.replace(name="edges_" + wq, T=T, K=K, E=len(EDGE_COUNTS), M_max=T)
+    wl = Workload(cfg)
+    wl.ids = routing_with_counts(EDGE_COUNTS, T, K)
+    lay = oracle_layout(wl)
+    assert list(lay["masked_m"][:len(EDGE_COUNTS)]) == EDGE_COUNTS
+    check_grouped_swiglu(wl)
+    check_grouped_down(wl)
+    L = wl.layer()
+    assert moe.moe_gemm_tile_rows(L.p, 3) == 128 and moe.moe_gemm_tile_rows(L.p, 4) == 128
+    lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
+    L.xg.copy_(to_dev(xg))
+    L.xg_s.copy_(to_dev(xgs))
+    L.masked_m.copy_(to_dev(lay["masked_m"]))
+    L.offsets.copy_(to_dev(lay["offsets"]))
+    L.swiglu()
+    torch.cuda.synchronize()
+    c = L.ws[:moe.MOE_STATS_BYTES].view(torch.int32).cpu().numpy().reshape(2, moe.MOE_STATS_CTAS, 2).sum(axis=1)
+    want = sum(-(-m // 128) for m in EDGE_COUNTS) + -(-T // 128)  # the shared slot holds all T rows
+    assert c[0, 1] == oracle.token_tiles(lay["masked_m"], 128) == want
 
 
 @pytest.mark.parametrize("name", [n for n in NAMES if SMALL[n].gemm != "f32"])
