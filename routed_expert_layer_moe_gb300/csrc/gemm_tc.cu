@@ -17,7 +17,9 @@
 //     Gate/up: the pair is the gate tile (rows [128j, 128j+128) of W1) and the
 //     up tile (same rows of W3).  Down: two consecutive 128-row tiles of W2.
 //     Units exist only for chunks with rows: each CTA builds the unit list from
-//     masked_m on the device at kernel start.
+//     masked_m on the device at kernel start.  A chunk's token box is the
+//     smallest of 16 / 32 / 64 / 128 rows that covers it (SM pairs: 128), so a
+//     decode expert with a few tokens reads no padding rows.
 //   * Two orientations:
 //       - token-major (every FP8 problem, and BF16 prefill): the 128 token rows
 //         are the MMA's M side and the gate and up tiles together one N = 256
