@@ -190,7 +190,7 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
 }
 
 // Token-major FP8 / FP4 units of one CTA with at most 64 token rows (decode-sized chunks) use
-// M = 64 MMAs: half the tensor time of M = 128 for rows that would only be padding.
+// M = 64 MMAs instead of 128-row ones whose extra rows would only be padding.
 template <bool F8, bool TM, bool PAIR>
 __device__ __forceinline__ bool m64_unit(const Unit& U) {
   return F8 && TM && !PAIR && U.nvalid <= 64;
