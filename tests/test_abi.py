@@ -122,3 +122,34 @@ def test_no_workspace_call_rejects_beyond_four_mib_without_gpu():
     p = moe.Problem.make(T=T, H=128, I=128, E=1024, K=8, layout="contig", act="f32", wt="f32", out="f32")
     r = L.moe_permute_no_workspace(ctypes.byref(p), fake, fake, None, fake, fake, fake, fake, fake, None, fake, None)
     assert r == moe.MOE_ERR_WORKSPACE
+
+
+def documented_tile_rows(T, H, K, P, wt, step):
+    """The header's rule for moe_gemm_tile_rows: 0 for fp32 experts (CUDA-core GEMM); 256 for FP8 /
+    FP4 experts with at least 128 rows per slot on average (T * K / P), and for step 4 only when H
+    is a multiple of 256; 128 otherwise."""
+    if wt == "f32":
+        return 0
+    if wt in ("e4m3", "e2m1") and T * K / P >= 128 and (step == 3 or H % 256 == 0):
+        return 256
+    return 128
+
+
+@pytest.mark.parametrize("T,H,I,E,K,P,S,wt,act,layout", [
+    (8192, 4096, 1024, 512, 10, 512, 0, "e4m3", "bf16", "contig"),    # prefill: SM pairs for both GEMMs
+    (8192, 4224, 1024, 512, 10, 512, 0, "e4m3", "bf16", "contig"),    # H not a multiple of 256: down on one CTA
+    (1024, 2048, 1024, 8, 1, 8, 0, "e2m1", "bf16", "contig"),         # exactly 128 rows per slot, FP4
+    (1016, 2048, 1024, 8, 1, 8, 0, "e2m1", "bf16", "contig"),         # just below
+    (128, 7168, 2048, 256, 8, 256, 1, "e4m3", "bf16", "masked"),      # DeepSeek-V3-shaped decode
+    (32, 4096, 14336, 8, 2, 8, 0, "bf16", "bf16", "masked"),          # Mixtral-shaped decode (bf16)
+    (8192, 4096, 1024, 64, 2, 64, 0, "bf16", "bf16", "contig"),       # bf16 prefill-sized: no pairs
+    (16, 64, 128, 8, 2, 8, 0, "f32", "f32", "masked"),                # fp32: CUDA cores
+])
+def test_gemm_tile_rows_follow_the_header_rule(T, H, I, E, K, P, S, wt, act, layout):
+    out = "f32" if wt == "f32" else "bf16"
+    p = moe.Problem.make(T=T, H=H, I=I, E=E, K=K, P=P, M_max=T if layout == "masked" else 0, has_shared=S,
+                         act=act, wt=wt, out=out, layout=layout)
+    assert moe.moe_check_problem(p) == moe.MOE_OK
+    for step in (3, 4):
+        assert moe.moe_gemm_tile_rows(p, step) == documented_tile_rows(T, H, K, P, wt, step), step
+    assert moe.moe_gemm_tile_rows(p, 5) == 0  # only steps 3 and 4 have a GEMM tile
