@@ -41,7 +41,8 @@ METRIC = "MoE layer tokens/s"
 # kernel source the capture was taken from; a changed kernel source gives no entry (null).
 TRAFFIC = {
     # ncu --metrics dram__bytes_read.sum,dram__bytes_write.sum (one pass) on the full-size workloads: the
-    # first launch of the dominant grouped GEMM kernel in a bench process
+    # first launch of the dominant grouped GEMM kernel in a bench process.  Taken on the kernel revision
+    # before FP8 / FP4 single-CTA launches moved to 64-row chunks; the present revision has no capture.
     "prefill:split:b6a55799c140746a": 4824612864 + 78791168,          # gate/up, SM pairs
     "mixtral_decode:ffn:b6a55799c140746a": 2821686528 + 5934080,      # one-launch FFN kernel (without the reduction)
     "dsv3_decode:split:b6a55799c140746a": 7491252480 + 8620800,       # gate/up

@@ -150,11 +150,13 @@ size_t moe_workspace_bytes(const moe_problem* p);
 /* Token rows BM of one tile of the tensor-core GEMM of step 3 (step = 3) or
  * step 4 (step = 4) for this problem ("Inference INFRA methodology (5)",
  * section "DeepGEMM": the tile height BM of the padding-waste ratio
- * ceil(M_e / BM) * BM / M_e).  128; or 256 for FP8 / FP4 experts with at least
- * 128 rows per slot on average (and, for step 4, H a multiple of 256): those
- * GEMMs run on pairs of SMs (thread-block clusters of two), each SM holding 128
- * of the tile's token rows and one of its two 128-row weight tiles, with one
- * cta_group::2 MMA over both.  moe_grouped_ffn always uses 128-row tiles.
+ * ceil(M_e / BM) * BM / M_e).  For bf16 experts 128.  For FP8 / FP4 experts
+ * 256 with at least 128 rows per slot on average (and, for step 4, H a multiple
+ * of 256): those GEMMs run on pairs of SMs (thread-block clusters of two), each
+ * SM holding 128 of the tile's token rows and one of its two 128-row weight
+ * tiles, with one cta_group::2 MMA over both; else 64: one CTA per SM with
+ * M = 64 MMAs.  moe_grouped_ffn runs on single CTAs: 64-row tiles for FP8 /
+ * FP4 experts, 128 for bf16.
  * 0 for an invalid problem or one whose GEMMs run on the CUDA cores (F32).
  * Host only; touches no GPU. */
 int32_t moe_gemm_tile_rows(const moe_problem* p, int32_t step);

@@ -413,12 +413,14 @@ __device__ __forceinline__ void tmem_ld32x2(uint32_t ta, uint32_t tb, float (&a)
   }
 }
 
-// One 32-lane x 32-column fp32 load from tensor memory, not waited for: the registers hold the
-// values only after tmem_wait_ld32 on the same array (which names them as operands, so the
-// compiler cannot read them earlier).
-__device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32]) {
+// One 16-lane load of 8 groups of 8 columns (tcgen05.ld 16x256b.x8) from the 16 lanes at ta, not
+// waited for (tmem_wait_ld32 on r): thread t gets lanes t/4 and t/4 + 8 of them, columns 2 (t % 4)
+// and 2 (t % 4) + 1 of each group, as r[4g] = (lane t/4, column 8g + 2 (t % 4)), r[4g + 1] = the
+// next column, r[4g + 2], r[4g + 3] = the same columns of lane t/4 + 8 (checked on a GB300 by
+// storing lane * 1000 + column with 32x32b stores and reading it back).
+__device__ __forceinline__ void tmem_ld16x256_x8(uint32_t ta, uint32_t (&r)[32]) {
   asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];\n"
       : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
       : "r"(ta)
       : "memory");
@@ -493,18 +495,6 @@ __device__ __forceinline__ uint64_t pair_of(float s) {
   uint64_t r;
   asm("mov.b64 %0, {%1, %1};" : "=l"(r) : "f"(s));
   return r;
-}
-
-// a[o .. o+31] += r[0..31] * s, as sixteen packed fp32x2 multiply-adds (two fmaf roundings each).
-__device__ __forceinline__ void fma2_chunk(float* a, const uint32_t (&r)[32], float s) {
-  const float2 sv = make_float2(s, s);
-#pragma unroll
-  for (int i = 0; i < 32; i += 2) {
-    const float2 v = __ffma2_rn(make_float2(__uint_as_float(r[i]), __uint_as_float(r[i + 1])), sv,
-                                make_float2(a[i], a[i + 1]));
-    a[i] = v.x;
-    a[i + 1] = v.y;
-  }
 }
 
 // Shared-memory matrix descriptor of a K-major tile written by TMA with the

@@ -12,8 +12,9 @@
 //
 // Design (GB300, one CTA per SM, persistent):
 //   * A unit is (slot s, token chunk c, tile pair j, K split q).  A slot's rows
-//     are split into ceil(rows/128) chunks of near-equal size, so the chunks of
-//     one expert take the same time and re-read its weights from L2 together.
+//     are split into chunks of near-equal size (at most 64 rows for FP8 / FP4 on
+//     one CTA, 128 for BF16, 256 on SM pairs), so the chunks of one expert take
+//     the same time and re-read its weights from L2 together.
 //     Gate/up: the pair is the gate tile (rows [128j, 128j+128) of W1) and the
 //     up tile (same rows of W3).  Down: two consecutive 128-row tiles of W2.
 //     Units exist only for chunks with rows: each CTA builds the unit list from
@@ -24,8 +25,11 @@
 //       - token-major (every FP8 problem, and BF16 prefill): the 128 token rows
 //         are the MMA's M side and the gate and up tiles together one N = 256
 //         MMA; the activation scale is one value per thread, and the SwiGLU, the
-//         e4m3 re-quantisation of h and the stores are row-local.  FP8 chunks of
-//         at most 64 rows use M = 64 MMAs (rows 16q..16q+15 in lane quarter q);
+//         e4m3 re-quantisation of h and the stores are row-local.  FP8 / FP4 on
+//         one CTA: chunks of at most 64 rows and M = 64 MMAs (rows 16q..16q+15
+//         in lane quarter q), read with 16x256b loads, so that each thread
+//         promotes two token rows and 32 values per tile and K block instead of
+//         one row of a 128-row tile that decode fills with padding;
 //       - weight-major (BF16 decode): the weight tile is the M = 128 side and the
 //         chunk's tokens the N side, rounded up to 16 -- an expert with a few
 //         tokens streams its weights at full width and issues N = 16 MMAs.
@@ -44,9 +48,8 @@
 //   * FP8: the MMAs of one 128-K block write one of two tensor-memory buffers;
 //     the epilogue reads it, scales it and adds it into fp32 registers while
 //     the MMA fills the other (SM pairs: the partial sums read as packed pairs
-//     and added with fp32x2 multiply-adds on paired accumulators; one CTA: four
-//     32-column chunks, each load issued before the previous chunk's
-//     multiply-adds -- each measured the faster of the two on its kernel).
+//     and added with fp32x2 multiply-adds on paired accumulators; one CTA: the
+//     16x256b form above).
 //     BF16: the whole K range accumulates in tensor memory; the two buffers
 //     alternate between units.
 //   * MODE_FFN runs gate/up and down in one cooperative launch: the unit list
@@ -81,6 +84,7 @@ constexpr int LOAD_WARP0 = 2;       // warps 2 and 3 load FP8 scales
 constexpr int LOAD_THREADS = 64;
 constexpr int RING = 32;            // K blocks of scales staged ahead of the epilogue
 constexpr int SG = 16;              // K blocks of scales fetched per loader pass (RING / 2: two groups in flight)
+constexpr int DEC_CH = 64;          // FP8 / FP4 on one CTA: token rows of one chunk at most (M = 64 MMAs)
 // Register split (setmaxnreg): warpgroup 0 (TMA, MMA, scale loads) gives
 // registers to the two epilogue warpgroups, which hold 2 x 64 fp32
 // accumulators per thread.  4*32*ctrl + 8*32*epi must not exceed
@@ -189,11 +193,23 @@ __device__ __forceinline__ Unit decode_unit(const TcParams& p, const Phase& f, i
   return U;
 }
 
-// Token-major FP8 / FP4 units of one CTA with at most 64 token rows (decode-sized chunks) use
-// M = 64 MMAs instead of 128-row ones whose extra rows would only be padding.
-template <bool F8, bool TM, bool PAIR>
-__device__ __forceinline__ bool m64_unit(const Unit& U) {
-  return F8 && TM && !PAIR && U.nvalid <= 64;
+// FP8 / FP4 on one CTA (64-row chunks, M = 64 MMAs): a[4g], a[4g + 1] += r[4g], r[4g + 1] * sa and
+// a[4g + 2], a[4g + 3] += r[4g + 2], r[4g + 3] * sb for the 8 groups of a 16x256b.x8 load (two token
+// rows with scales sa and sb), as packed fp32x2 multiply-adds (each element rounded as the scalar
+// fmaf would)
+__device__ __forceinline__ void promote_rows2(float* a, const uint32_t (&r)[32], float sa, float sb) {
+  const float2 va = make_float2(sa, sa), vb = make_float2(sb, sb);
+#pragma unroll
+  for (int g = 0; g < 8; ++g) {
+    const float2 q0 = __ffma2_rn(make_float2(__uint_as_float(r[4 * g]), __uint_as_float(r[4 * g + 1])), va,
+                                 make_float2(a[4 * g], a[4 * g + 1]));
+    const float2 q1 = __ffma2_rn(make_float2(__uint_as_float(r[4 * g + 2]), __uint_as_float(r[4 * g + 3])), vb,
+                                 make_float2(a[4 * g + 2], a[4 * g + 3]));
+    a[4 * g] = q0.x;
+    a[4 * g + 1] = q0.y;
+    a[4 * g + 2] = q1.x;
+    a[4 * g + 3] = q1.y;
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float a, float b) {
@@ -258,7 +274,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // tmA / tmB*: weights and token boxes of phase 0; tmA2 / tmC*: those of phase 1 (MODE_FFN)
   static_assert(TM || !F8, "FP8 / FP4 run token-major");
   static_assert(!PAIR || (F8 && TM && MODE != MODE_FFN), "SM pairs: FP8 / FP4 token-major, one GEMM per launch");
-  constexpr int CH = PAIR ? 2 * BN : BN;  // token rows of one chunk at most
+  // FP8 / FP4 on one CTA: 64-row chunks, M = 64 MMAs, the 16x256b promotion (see the epilogue)
+  constexpr bool DEC = F8 && TM && !PAIR;
+  constexpr int CH = PAIR ? 2 * BN : DEC ? DEC_CH : BN;  // token rows of one chunk at most
   constexpr uint32_t SB = PAIR ? TILE_A_BYTES + TILE_B_BYTES : STAGE_BYTES;  // bytes of one pipeline stage
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~(uintptr_t)1023);
@@ -352,7 +370,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // other CTAs wrote; wait (bounded) until every gate/up unit of slot s has released them.
   auto wait_ready = [&](int s) -> bool {
     const int m = srows[s];
-    const int need = ((m + BN - 1) / BN) * p.ph[0].pairs * p.ph[0].ksplit * EPI_WARPS;  // one release per epilogue warp
+    const int need = ((m + CH - 1) / CH) * p.ph[0].pairs * p.ph[0].ksplit * EPI_WARPS;  // one release per epilogue warp
     const long long t0 = clock64();
     while (ld_acquire_gpu(p.ready + s) < need) {
       if (*abort_flag) return false;
@@ -502,7 +520,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // (token-major: the weights are the B operand, of format w_fmt)
           // (token-major FP8 / FP4: the weights are the B operand, of format w_fmt)
           const uint32_t idesc = PAIR ? (mma_idesc<F8>(2 * BM, 2 * BM) | (p.w_fmt << 10))
-                                 : TM ? (mma_idesc<F8>(m64_unit<F8, TM, PAIR>(U) ? 64 : BM, U.a1 ? 2 * BM : BM) |
+                                 : TM ? (mma_idesc<F8>(DEC ? DEC_CH : BM, U.a1 ? 2 * BM : BM) |
                                          (F8 ? p.w_fmt << 10 : 0u))
                                       : mma_idesc<F8>(BM, (U.nvalid + 15) & ~15);
           uint32_t b = 0;
@@ -703,11 +721,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const size_t oc = (size_t)f.out_cols;
       const int nkb = U.kb1 - U.kb0;
       const bool split = f.ksplit > 1;
-      // M = 64 units (m64_unit): accumulator row r sits in lane 32 (r / 16) + r % 16, so thread
-      // (quarter q, lane l < 16) holds token row 16 q + l and lanes 16-31 of each quarter hold none
-      const bool m64 = m64_unit<F8, TM, PAIR>(U);
-      const bool evalid = !m64 || lane < 16;
-      const int erow = m64 ? (lane < 16 ? quarter * 16 + lane : 0) : lrow;  // token row of this thread
+      // FP8 / FP4 on one CTA: the M = 64 accumulator row r sits in lane 32 (r / 16) + r % 16; each
+      // warp reads its quarter's 16 rows with 16x256b loads, so thread t holds token rows
+      // mr0 = 16 q + t / 4 and mr1 = mr0 + 8, columns c_lo + 8 g + mc and the next one of every
+      // 8-column group g (half the values of a 32x32b read of 128 lanes, none of them padding lanes)
+      const int mr0 = quarter * 16 + (lane >> 2), mr1 = mr0 + 8, mc = 2 * (lane & 3);
       if (h == 1) release_pending();
       // weight-major: this thread owns weight row lrow of each tile and token columns
       // [c_lo, c_lo + ncols); token-major: token row lrow and weight columns [64*half, +64)
@@ -744,9 +762,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           tc_fence_after_sync();
           const int slot = (int)gh * SG + j;
-          const float xs = sx[slot * BN + erow];
-          const float s0 = sw[slot * 2] * xs, s1 = sw[slot * 2 + 1] * xs;
           if constexpr (PAIR) {
+            const float xs = sx[slot * BN + lrow];
+            const float s0 = sw[slot * 2] * xs, s1 = sw[slot * 2 + 1] * xs;
             // SM pairs: two steps of 64 columns (tile 0 and tile 1, columns c_lo.. then c_lo+32..),
             // loaded as packed pairs and added with fp32x2 multiply-adds on paired accumulators;
             // the buffer is handed back once the second step is loaded, before its multiply-adds
@@ -769,27 +787,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               fma2_pairs<16>(accp1 + pr * 16, v + 16, p1);
             }
           } else {
-            const float p0 = s0, p1 = s1;
-            // one CTA: four 32-column chunks (tile 0 cols c_lo.., tile 1 cols c_lo.., tile 0 cols
-            // c_lo+32.., tile 1 cols c_lo+32..), each load issued before the multiply-adds of the previous
-            // chunk so that its latency hides behind them
+            // one CTA: 64 columns of each tile, 32 values a thread (two token rows); the buffer is
+            // handed back once loaded, before the multiply-adds
             uint32_t ra[32], rb[32];
             const uint32_t c0 = t_lane + b * 256u + (uint32_t)c_lo;
-            tmem_ld32(c0, ra);
+            tmem_ld16x256_x8(c0, ra);
+            tmem_ld16x256_x8(c0 + 128u, rb);
             tmem_wait_ld32(ra);
-            tmem_ld32(c0 + 128u, rb);
-            fma2_chunk(acc0, ra, p0);
             tmem_wait_ld32(rb);
-            tmem_ld32(c0 + 32u, ra);
-            fma2_chunk(acc1, rb, p1);
-            tmem_wait_ld32(ra);
-            tmem_ld32(c0 + 160u, rb);
-            fma2_chunk(acc0 + 32, ra, p0);
-            tmem_wait_ld32(rb);
-            // the buffer is read: hand it back before the last multiply-adds
             tc_fence_before_sync();
             warp_arrive(&tempty[b]);
-            fma2_chunk(acc1 + 32, rb, p1);
+            const float w0 = sw[slot * 2], w1 = sw[slot * 2 + 1];
+            const float xa = sx[slot * BN + mr0], xb = sx[slot * BN + mr1];
+            promote_rows2(acc0, ra, w0 * xa, w0 * xb);
+            promote_rows2(acc1, rb, w1 * xa, w1 * xb);
           }
           if (j == SG - 1 || k == nkb - 1) {  // the group's scales are no longer read
             warp_arrive(&gempty[gh]);
@@ -833,13 +844,99 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ++acc_it;
       }
 
+      if constexpr (DEC) {
+        // acc0 / acc1 [4g], [4g + 1] = row mr0, columns c_lo + 8g + mc (+ 1) of tile 0 / 1;
+        // [4g + 2], [4g + 3] = the same columns of row mr1
+        {
+          const bool v0 = mr0 < U.nvalid, v1 = mr1 < U.nvalid;
+          if (split) {
+            float* pq = f.part + (size_t)U.q * p.rows_total * oc + (size_t)U.j * f.pair_stride + c_lo + mc;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (v0) {
+                float* d = pq + (size_t)(U.rowB + mr0) * oc + 8 * g;
+                *reinterpret_cast<float2*>(d) = make_float2(acc0[4 * g], acc0[4 * g + 1]);
+                if (U.a1) *reinterpret_cast<float2*>(d + BM) = make_float2(acc1[4 * g], acc1[4 * g + 1]);
+              }
+              if (v1) {
+                float* d = pq + (size_t)(U.rowB + mr1) * oc + 8 * g;
+                *reinterpret_cast<float2*>(d) = make_float2(acc0[4 * g + 2], acc0[4 * g + 3]);
+                if (U.a1) *reinterpret_cast<float2*>(d + BM) = make_float2(acc1[4 * g + 2], acc1[4 * g + 3]);
+              }
+            }
+            continue;
+          }
+          release_pending();
+          if (mode == MODE_SWIGLU) {
+            // e4m3 per 1x128 group: a row's 128 columns of tile j sit in the four threads of a quad
+            // of both column halves
+            float hv[32];
+#pragma unroll
+            for (int i = 0; i < 32; ++i) hv[i] = silu(acc0[i]) * acc1[i];
+            float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              a0 = fmaxf(a0, fmaxf(fabsf(hv[4 * g]), fabsf(hv[4 * g + 1])));
+              a1 = fmaxf(a1, fmaxf(fabsf(hv[4 * g + 2]), fabsf(hv[4 * g + 3])));
+            }
+#pragma unroll
+            for (int off = 1; off < 4; off <<= 1) {
+              a0 = fmaxf(a0, __shfl_xor_sync(0xffffffffu, a0, off));
+              a1 = fmaxf(a1, __shfl_xor_sync(0xffffffffu, a1, off));
+            }
+            float* redp = red + (size_t)(u_it & 1u) * 512;  // [2 halves][128 rows]
+            if ((lane & 3) == 0) {
+              redp[half * 128 + mr0] = a0;
+              redp[half * 128 + mr1] = a1;
+            }
+            if (!epi_sync()) break;
+            const float m0 = fmaxf(redp[mr0], redp[128 + mr0]), m1 = fmaxf(redp[mr1], redp[128 + mr1]);
+            const float sc0 = (m0 == 0.0f) ? 1.0f : __fdiv_rn(m0, 448.0f);
+            const float sc1 = (m1 == 0.0f) ? 1.0f : __fdiv_rn(m1, 448.0f);
+            const float i0 = 1.0f / sc0, i1 = 1.0f / sc1;
+            uint8_t* o8 = static_cast<uint8_t*>(f.out) + (size_t)U.j * BM + c_lo + mc;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (v0)
+                *reinterpret_cast<__nv_fp8x2_storage_t*>(o8 + (size_t)(U.rowB + mr0) * oc + 8 * g) =
+                    __nv_cvt_float2_to_fp8x2(make_float2(hv[4 * g] * i0, hv[4 * g + 1] * i0), __NV_SATFINITE,
+                                             __NV_E4M3);
+              if (v1)
+                *reinterpret_cast<__nv_fp8x2_storage_t*>(o8 + (size_t)(U.rowB + mr1) * oc + 8 * g) =
+                    __nv_cvt_float2_to_fp8x2(make_float2(hv[4 * g + 2] * i1, hv[4 * g + 3] * i1), __NV_SATFINITE,
+                                             __NV_E4M3);
+            }
+            if (half == 0 && (lane & 3) == 0) {
+              if (v0) f.out_scales[(size_t)(U.rowB + mr0) * (oc / 128) + U.j] = sc0;
+              if (v1) f.out_scales[(size_t)(U.rowB + mr1) * (oc / 128) + U.j] = sc1;
+            }
+          } else {
+            __nv_bfloat16* o = static_cast<__nv_bfloat16*>(f.out) + (size_t)U.j * f.pair_stride + c_lo + mc;
+#pragma unroll
+            for (int g = 0; g < 8; ++g) {
+              if (v0) {
+                __nv_bfloat16* d = o + (size_t)(U.rowB + mr0) * oc + 8 * g;
+                *reinterpret_cast<uint32_t*>(d) = pack_bf16x2(acc0[4 * g], acc0[4 * g + 1]);
+                if (U.a1) *reinterpret_cast<uint32_t*>(d + BM) = pack_bf16x2(acc1[4 * g], acc1[4 * g + 1]);
+              }
+              if (v1) {
+                __nv_bfloat16* d = o + (size_t)(U.rowB + mr1) * oc + 8 * g;
+                *reinterpret_cast<uint32_t*>(d) = pack_bf16x2(acc0[4 * g + 2], acc0[4 * g + 3]);
+                if (U.a1) *reinterpret_cast<uint32_t*>(d + BM) = pack_bf16x2(acc1[4 * g + 2], acc1[4 * g + 3]);
+              }
+            }
+          }
+          if (MODE == MODE_FFN && mode == MODE_SWIGLU) pending = U.s;  // released later (see release_pending)
+          continue;
+        }
+      } else {
       if (split) {
         // this split's fp32 partial sums go to the dense [split][row][column] workspace; a
         // separate reduction kernel adds the splits in split order (no atomics, no waits)
         float* pq = f.part + (size_t)U.q * p.rows_total * oc;
         if constexpr (TM) {
-          if (evalid && erow < U.nvalid) {
-            float* prow = pq + (size_t)(U.rowB + erow) * oc + (size_t)U.j * f.pair_stride + c_lo;
+          if (lrow < U.nvalid) {
+            float* prow = pq + (size_t)(U.rowB + lrow) * oc + (size_t)U.j * f.pair_stride + c_lo;
             const bool wide = (reinterpret_cast<uintptr_t>(f.part) & 31u) == 0;  // offsets are 256-byte multiples
             store_f32x64(prow, acc0, wide);
             if (U.a1) store_f32x64(prow + BM, acc1, wide);
@@ -862,8 +959,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // ---- final values of this unit
       float* redp = red + (size_t)(u_it & 1u) * 512;  // maxima, double-buffered by unit parity
       if constexpr (TM) {
-        const bool row_ok = evalid && erow < U.nvalid;
-        const size_t row = (size_t)(U.rowB + erow);
+        const bool row_ok = lrow < U.nvalid;
+        const size_t row = (size_t)(U.rowB + lrow);
         if (mode == MODE_SWIGLU) {
           // rows past the chunk hold other tokens' data: no SwiGLU, no store
           if (row_ok) {
@@ -934,6 +1031,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (MODE == MODE_FFN && mode == MODE_SWIGLU) pending = U.s;  // released later (see release_pending)
+      }
     }
     release_pending();
   }
@@ -1118,13 +1216,14 @@ Plan make_plan(const moe_problem& p, int mode, int sm_count, int smem_cap, int n
   const double rows_per_slot = (double)p.T * p.K / std::max(1, p.P);
   pl.tm = f8 || rows_per_slot >= 64.0;
   pl.pair = use_pairs(p, mode, nphase);
+  const int ch = pl.pair ? 2 * BN : f8 ? DEC_CH : BN;  // token rows of one chunk at most
   // upper bound of the token chunks over all slots
   long chunks;
   if (p.layout == MOE_LAYOUT_MASKED) {
-    chunks = (long)pl.nslots * ((p.M_max + BN - 1) / BN);
+    chunks = (long)pl.nslots * ((p.M_max + ch - 1) / ch);
   } else {
     const long rows = (long)p.T * p.K + (long)p.has_shared * p.T;
-    chunks = std::min<long>((long)pl.nslots * ((p.T + BN - 1) / BN), pl.nslots + rows / BN);
+    chunks = std::min<long>((long)pl.nslots * ((p.T + ch - 1) / ch), pl.nslots + rows / ch);
   }
   const long tiles = chunks * pl.pairs;
   pl.ksplit = 1;
@@ -1465,7 +1564,7 @@ __global__ void __launch_bounds__(256) grouped_gemm_f32_kernel(const float* __re
 
 int gemm_tile_rows(const moe_problem& p, int mode) {
   if (p.wt == MOE_F32) return 0;
-  return use_pairs(p, mode, 1) ? 2 * BN : BN;
+  return use_pairs(p, mode, 1) ? 2 * BN : fp8_acts(p) ? DEC_CH : BN;
 }
 
 size_t gemm_workspace_bytes(const moe_problem& p) {

@@ -125,19 +125,19 @@ def test_no_workspace_call_rejects_beyond_four_mib_without_gpu():
 
 
 def documented_tile_rows(T, H, K, P, wt, step):
-    """The header's rule for moe_gemm_tile_rows: 0 for fp32 experts (CUDA-core GEMM); 256 for FP8 /
-    FP4 experts with at least 128 rows per slot on average (T * K / P), and for step 4 only when H
-    is a multiple of 256; 128 otherwise."""
+    """The header's rule for moe_gemm_tile_rows: 0 for fp32 experts (CUDA-core GEMM); for FP8 / FP4
+    experts 256 with at least 128 rows per slot on average (T * K / P; for step 4 only when H is
+    a multiple of 256), else 64; 128 for bf16 experts."""
     if wt == "f32":
         return 0
-    if wt in ("e4m3", "e2m1") and T * K / P >= 128 and (step == 3 or H % 256 == 0):
-        return 256
+    if wt in ("e4m3", "e2m1"):
+        return 256 if T * K / P >= 128 and (step == 3 or H % 256 == 0) else 64
     return 128
 
 
 @pytest.mark.parametrize("T,H,I,E,K,P,S,wt,act,layout", [
     (8192, 4096, 1024, 512, 10, 512, 0, "e4m3", "bf16", "contig"),    # prefill: SM pairs for both GEMMs
-    (8192, 4224, 1024, 512, 10, 512, 0, "e4m3", "bf16", "contig"),    # H not a multiple of 256: down on one CTA
+    (8192, 4224, 1024, 512, 10, 512, 0, "e4m3", "bf16", "contig"),    # H not a multiple of 256: down on one CTA (64)
     (1024, 2048, 1024, 8, 1, 8, 0, "e2m1", "bf16", "contig"),         # exactly 128 rows per slot, FP4
     (1016, 2048, 1024, 8, 1, 8, 0, "e2m1", "bf16", "contig"),         # just below
     (128, 7168, 2048, 256, 8, 256, 1, "e4m3", "bf16", "masked"),      # DeepSeek-V3-shaped decode

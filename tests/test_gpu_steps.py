@@ -411,18 +411,19 @@ def routing_with_counts(counts, T, K):
     return ids
 
 
-# slot row counts on both sides of every token box (16 / 32 / 64 / 128 rows) and of the split of a
-# slot into two chunks (above 128 rows), plus an empty slot
+# slot row counts on both sides of every token box (16 / 32 / 64 rows) and of the splits of a slot
+# into two and three chunks (above 64 and 128 rows), plus an empty slot
 EDGE_COUNTS = [0, 1, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 47]
 
 
 @pytest.mark.parametrize("wq", ["e4m3", "e2m1"])
 def test_grouped_gemms_at_token_box_edges(wq):
-    """FP8 / FP4 decode-shaped GEMMs (token-major, one CTA per SM) on a layout whose slots hold
-    0, 1, 15-17, 31-33, 63-65 and 127-129 rows (and a shared expert with every token): the token
-    box of each chunk is the smallest of 16 / 32 / 64 / 128 rows covering it, and the MMA reads
-    stale shared memory past the box.  Values within tolerance of the oracle, padding rows
-    untouched, token tiles = sum over slots of ceil(rows / 128)."""
+    """FP8 / FP4 decode-shaped GEMMs (token-major, one CTA per SM: chunks of at most 64 rows,
+    M = 64 MMAs) on a layout whose slots hold 0, 1, 15-17, 31-33, 63-65 and 127-129 rows (and a
+    shared expert with every token): the token box of each chunk is the smallest of 16 / 32 / 64
+    rows covering it, the MMA reads stale shared memory past the box, and slots above 64 rows
+    split into two or three chunks.  Values within tolerance of the oracle, padding rows
+    untouched, token tiles = sum over slots of ceil(rows / 64)."""
     T, K = 192, 4
     base = SMALL["e4m3_masked_shared"] if wq == "e4m3" else SMALL["e2m1_masked_shared"]
     cfg = base.replace(name="edges_" + wq, T=T, K=K, E=len(EDGE_COUNTS), M_max=T)
@@ -433,7 +434,7 @@ def test_grouped_gemms_at_token_box_edges(wq):
     check_grouped_swiglu(wl)
     check_grouped_down(wl)
     L = wl.layer()
-    assert moe.moe_gemm_tile_rows(L.p, 3) == 128 and moe.moe_gemm_tile_rows(L.p, 4) == 128
+    assert moe.moe_gemm_tile_rows(L.p, 3) == 64 and moe.moe_gemm_tile_rows(L.p, 4) == 64
     lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
     L.xg.copy_(to_dev(xg))
     L.xg_s.copy_(to_dev(xgs))
@@ -442,23 +443,24 @@ def test_grouped_gemms_at_token_box_edges(wq):
     L.swiglu()
     torch.cuda.synchronize()
     c = L.ws[:moe.MOE_STATS_BYTES].view(torch.int32).cpu().numpy().reshape(2, moe.MOE_STATS_CTAS, 2).sum(axis=1)
-    want = sum(-(-m // 128) for m in EDGE_COUNTS) + -(-T // 128)  # the shared slot holds all T rows
-    assert c[0, 1] == oracle.token_tiles(lay["masked_m"], 128) == want
+    want = sum(-(-m // 64) for m in EDGE_COUNTS) + -(-T // 64)  # the shared slot holds all T rows
+    assert c[0, 1] == oracle.token_tiles(lay["masked_m"], 64) == want
 
 
 @pytest.mark.parametrize("name", [n for n in NAMES if SMALL[n].gemm != "f32"])
 def test_gemm_issue_counters(workloads, name):
     """The GEMMs' token tiles (summed over CTAs from the counters in the workspace) equal the
-    oracle's sum over slots of ceil(masked_m / BM), BM the GEMM's tile height (128, or 256 on SM
-    pairs): no tile for padding rows or empty slots; every unit belongs to one such tile
-    (units = tiles x tile pairs x K splits).  The one-launch FFN uses 128-row tiles."""
+    oracle's sum over slots of ceil(masked_m / BM), BM the GEMM's tile height (64 for FP8 / FP4
+    on one CTA, 128 for bf16, 256 on SM pairs): no tile for padding rows or empty slots; every
+    unit belongs to one such tile (units = tiles x tile pairs x K splits).  The one-launch FFN
+    runs on single CTAs: 64-row tiles for FP8 / FP4, 128 for bf16."""
     wl = workloads[name]
     cfg = wl.cfg
     lay, xg, xgs, w13, w13s, w2, w2s = gemm_inputs(wl)
     L = wl.layer()
     bm = {3: moe.moe_gemm_tile_rows(L.p, 3), 4: moe.moe_gemm_tile_rows(L.p, 4)}
-    assert bm[3] in (128, 256) and bm[4] in (128, 256)
-    want = oracle.token_tiles(lay["masked_m"], 128)
+    assert bm[3] in (64, 128, 256) and bm[4] in (64, 128, 256)
+    want = oracle.token_tiles(lay["masked_m"], 64 if bm[3] == 256 else bm[3])
     L.xg.copy_(to_dev(xg))
     if xgs is not None:
         L.xg_s.copy_(to_dev(xgs))
