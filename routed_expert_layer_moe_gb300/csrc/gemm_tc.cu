@@ -724,11 +724,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // FP8 / FP4 on one CTA: the M = 64 accumulator row r sits in lane 32 (r / 16) + r % 16; each
       // warp reads its quarter's 16 rows with 16x256b loads, so thread t holds token rows
       // mr0 = 16 q + t / 4 and mr1 = mr0 + 8, columns c_lo + 8 g + mc and the next one of every
-      // 8-column group g (half the values of a 32x32b read of 128 lanes, none of them padding lanes)
+      // 8-column group g (half the values of a 32x32b read of all 128 lanes, and none from the
+      // lanes the M = 64 layout leaves empty)
       const int mr0 = quarter * 16 + (lane >> 2), mr1 = mr0 + 8, mc = 2 * (lane & 3);
       if (h == 1) release_pending();
       // weight-major: this thread owns weight row lrow of each tile and token columns
-      // [c_lo, c_lo + ncols); token-major: token row lrow and weight columns [64*half, +64)
+      // [c_lo, c_lo + ncols); token-major (BF16, SM pairs): token row lrow and weight columns
+      // [64*half, +64); FP8 / FP4 on one CTA: rows mr0, mr1 within the same columns
       const int c_lo = half * 64;
       const int ncols = TM ? 64 : max(0, min(64, U.nvalid - c_lo));
       const int npair = (ncols + 31) >> 5;  // 32-column loads
